@@ -1,0 +1,99 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake (a dropped term, a wrong sign, a swapped
+operand or coefficient, a misplaced restart, a lost transpose or safety
+factor) into a private copy of the oracle's source, on the CPU, and checks
+that at least one pin fails for the mutant while all pass for the original.
+"""
+import importlib.util
+import os
+import sys
+
+import numpy as np
+import pytest
+
+from inputs import generators as gen
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "gram_ns.py")
+
+MUTANTS = {
+    "drop_aR_in_RZ": ("RZ = _mm(counter, R, Z, symmetric=True) + a * R",
+                      "RZ = _mm(counter, R, Z, symmetric=True)"),
+    "sign_aRZ": ("R = _mm(counter, Z, RZ, symmetric=True) + a * RZ",
+                 "R = _mm(counter, Z, RZ, symmetric=True) - a * RZ"),
+    "drop_aI_at_reset": ("Q = Z + a * I\n", "Q = Z\n"),
+    "wrong_operand_in_Q": ("Q = _mm(counter, Q, Z, symmetric=True) + a * Q",
+                           "Q = _mm(counter, Q, Z, symmetric=True) + a * Z"),
+    "swap_b_c": ("Z = b * R + c * _mm(counter, R, R, symmetric=True)",
+                 "Z = c * R + b * _mm(counter, R, R, symmetric=True)"),
+    "restart_one_late": ("if (t - 1) in restarts:", "if (t - 2) in restarts:"),
+    "no_safety_factor": ('return X / (SAFETY * (np.linalg.norm(X, "fro") + EPS))',
+                         'return X / (np.linalg.norm(X, "fro") + EPS)'),
+    "transposed_gram": ("    R = _mm(counter, X, X.T, symmetric=True)\n    Q = None  # identity; the first",
+                        "    R = _mm(counter, X.T, X, symmetric=True)[:X.shape[0], :X.shape[0]]\n    Q = None  # identity; the first"),
+    "restart_uses_old_Q_transposed": ("            X = _mm(counter, Q, X)\n",
+                                      "            X = _mm(counter, Q.T @ Q, X)\n"),
+    "std_ns_drop_aX": ("X = a * X + _mm(counter, B, X)", "X = _mm(counter, B, X)"),
+    "naive_R_update_order": ("R = _mm(counter, ZR, Z, symmetric=True)",
+                             "R = _mm(counter, ZR, ZR, symmetric=True)"),
+    "lost_back_transpose": ("    out = _mm(counter, Q, X)\n    return out.T if transposed else out\n\n\ndef orthogonalize(",
+                            "    out = _mm(counter, Q, X)\n    return out\n\n\ndef orthogonalize("),
+    "skip_R_update_always": ("if t < steps and t not in restarts:", "if t < steps - 1 and t not in restarts:"),
+}
+
+
+def load_variant(name, source):
+    spec = importlib.util.spec_from_loader(name, loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    exec(compile(source, name, "exec"), mod.__dict__)
+    return mod
+
+
+def closed_form(X, O):
+    U, S, Vt = np.linalg.svd(X, full_matrices=False)
+    s_hat = S / (1.05 * (np.linalg.norm(X) + 1e-7))
+    p = s_hat.copy()
+    for _ in range(5):
+        a, b, c = 3.4445, -4.7750, 2.0315
+        p = a * p + b * p ** 3 + c * p ** 5
+    return (U * p) @ Vt
+
+
+def pins_pass(O):
+    """A battery of the oracle pins; True when every one holds."""
+    try:
+        for shape in ((8, 32), (24, 10), (6, 6)):
+            X = gen.gaussian(*shape, seed=31).astype(np.float64)
+            want = closed_form(X, O)
+            for out in (O.gram_ns(X), O.standard_ns(X), O.gram_ns_naive(X), O.orthogonalize(X)):
+                if out.shape != want.shape:
+                    return False
+                if np.linalg.norm(out - want) > 1e-10 * np.linalg.norm(want):
+                    return False
+        trace = []
+        O.gram_ns(gen.gaussian(8, 24, seed=1).astype(np.float64), trace=trace)
+        seq = [(t, n) for t, n, _ in trace]
+        if seq != [(0, "R"), (1, "Z"), (1, "Q"), (1, "RZ"), (1, "R"), (2, "Z"), (2, "Q"),
+                   (3, "X"), (3, "R"), (3, "Z"), (3, "Q"), (3, "RZ"), (3, "R"),
+                   (4, "Z"), (4, "Q"), (4, "RZ"), (4, "R"), (5, "Z"), (5, "Q")]:
+            return False
+        n, m = 16, 64
+        c = O.FlopCounter()
+        O.gram_ns(gen.gaussian(n, m, seed=2).astype(np.float64), counter=c)
+        if c.flops != (4 * 5 + 6 * 4 - 6) * n ** 3:
+            return False
+    except Exception:
+        return False
+    return True
+
+
+def test_original_passes():
+    assert pins_pass(load_variant("oracle_original", open(SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    src = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site not unique/found: {name}"
+    assert not pins_pass(load_variant(f"oracle_{name}", src.replace(old, new)))
