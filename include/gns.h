@@ -1,0 +1,172 @@
+/*
+ * gns.h: C ABI of the GB300 (sm_103a) Gram Newton-Schulz / Muon library.
+ *
+ * Every entry point is plain C: device or host pointers, sizes, scalars and a
+ * CUDA stream passed as void* (cudaStream_t; NULL means the legacy default
+ * stream). No call allocates caller-visible memory. Calls that take device
+ * pointers are asynchronous on `stream` unless stated otherwise.
+ *
+ * Ownership: the caller owns every buffer it passes. The library owns one
+ * cached workspace per device (Gram state, fp16 copies of the inputs, norm
+ * partials, a status word). It grows on demand and is freed by
+ * gns_release(). Calls on different streams of one device must not overlap
+ * in time, because they share that workspace.
+ *
+ * Errors: argument and shape errors, and failures of CUDA runtime calls, are
+ * returned at once as a negative gns_status. Conditions found on the device
+ * (a non-finite input norm, a bounded wait that ran out) set a per-device
+ * status word that gns_get_status() reads.
+ *
+ * Notation: a matrix X of R x C is handled as n x m with n = min(R, C),
+ * m = max(R, C); a matrix with R > C is transposed on the way in and back on
+ * the way out. Citations are to "Dion3: Full-stack orthogonal updates"
+ * (arXiv 2608.11612) and to the grouped Muon kernel card
+ * (kernels/phanerozoic/muon).
+ */
+#ifndef GNS_H
+#define GNS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GNS_OK = 0,
+    GNS_ERR_INVALID = -1,     /* bad argument (null pointer, size, steps, alignment) */
+    GNS_ERR_CUDA = -2,        /* a CUDA runtime call failed; see gns_last_error() */
+    GNS_ERR_NONFINITE = -3,   /* device: some input matrix had a non-finite norm */
+    GNS_ERR_TIMEOUT = -4,     /* device: a bounded wait inside a kernel ran out */
+    GNS_ERR_NOMEM = -5,       /* the workspace could not be allocated */
+    GNS_ERR_UNSUPPORTED = -6  /* the current device is not an sm_103 (GB300) GPU */
+} gns_status;
+
+/* Default (and maximum) number of Newton-Schulz steps a call accepts. */
+#define GNS_MAX_STEPS 64
+
+/*
+ * gns_orthogonalize_batched: approximate polar(X) for each of G matrices.
+ *
+ * Follows Dion3 §4.2 Algorithm 3 (stabilized Gram Newton-Schulz) with the
+ * a-term distribution of App. B.2.3, and, for square matrices, the standard
+ * iteration of §2.2 Algorithm 1 with symmetric products (App. C.3), as §4.1
+ * prescribes for alpha = 1. Each matrix is scaled to Frobenius norm 1/1.05
+ * (App. B.2.2 safety factor; X / (1.05 (||X||_F + 1e-7))), cast to fp16 and
+ * iterated in fp16 storage with fp32 accumulation.
+ *
+ *   ptr        device fp32 [G][R][C], row-major, contiguous. Overwritten in
+ *              place with the result (fp32, same shape).
+ *   G, R, C    G >= 0 (G == 0 is a no-op), R >= 1, C >= 1.
+ *   steps      1..GNS_MAX_STEPS (5 in the pages' setting).
+ *   restart_at restart period p: restart after every step t with t % p == 0
+ *              and steps - t >= p (p = 2, steps = 5 gives Algorithm 3's single
+ *              restart after step 2; p <= 0 never restarts). Ignored for
+ *              square matrices.
+ *   coeffs     HOST float[3*steps], (a_t, b_t, c_t) for t = 1..steps, or
+ *              NULL for the constant quintic (3.4445, -4.7750, 2.0315) of the
+ *              Muon kernel card at every step. Non-finite values are rejected.
+ *   stream     cudaStream_t.
+ * Returns GNS_OK or a negative gns_status. Asynchronous.
+ */
+int gns_orthogonalize_batched(float* ptr, int G, int R, int C, int steps, int restart_at,
+                              const float* coeffs, void* stream);
+
+/*
+ * gns_orthogonalize_batched_host: the same computation on a HOST buffer.
+ * host_ptr is fp32 [G][R][C] in host memory (pinned memory gives full copy
+ * speed); the library copies it to a device staging buffer it owns, runs
+ * gns_orthogonalize_batched there, copies the result back and synchronizes
+ * `stream` before returning.
+ */
+int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int steps,
+                                   int restart_at, const float* coeffs, void* stream);
+
+/* One 2D tensor of a Muon step. data is a device pointer; rows x cols,
+ * row-major, contiguous. base_index is the global index of element (0, 0)
+ * for the stochastic-rounding counter (the Muon kernel card: a parameter
+ * updated whole or across shards rounds identically). */
+typedef struct {
+    void* data;
+    int rows;
+    int cols;
+    int64_t base_index;
+} gns_tensor;
+
+/*
+ * muon_step: one Muon step over n weight matrices (Dion3 §2.1 Eq. 1 with
+ * decoupled weight decay, §6 "Weight Update"; the Muon kernel card):
+ *   M <- mu M + G                              (fp32, M_0 = 0)
+ *   O <- gns(M)                                (as gns_orthogonalize_batched,
+ *                                               steps 5, restart_at 2, quintic)
+ *   W <- SR_bf16((1 - lr*wd) W - lr*s*O),  s = 0.2 sqrt(max(rows, cols))
+ * with the update in fp32 (decay = 1 - lr*wd, step = lr*s,
+ * w' = decay*w - step*o, each rounded once) and a stochastically rounded
+ * bf16 write-back keyed by (seed, step, base_index + element index)
+ * (Philox4x32-10; element i uses the low 16 bits of output word (g & 3) of
+ * the block g >> 2, g = base_index + i).
+ *
+ *   params    n tensors, bf16 weights, updated in place.
+ *   grads     n tensors, bf16 gradients (same shapes), read.
+ *   momentum  n tensors, fp32 momentum (same shapes), updated in place.
+ * Matrices are grouped into buckets of equal (rows, cols) and each bucket is
+ * orthogonalized in one batched pass. Returns GNS_OK or a negative status.
+ */
+int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum,
+              int n, float lr, float wd, float mu, uint64_t seed, uint64_t step, void* stream);
+
+/*
+ * gns_muon_momentum: the first elementwise pass of muon_step on one tensor:
+ * M <- mu*M + float(G), fp32, two roundings (Dion3 Eq. 1).
+ *   M      device fp32 [numel], updated in place.
+ *   G_bf16 device bf16 bits [numel].
+ */
+int gns_muon_momentum(float* M, const uint16_t* G_bf16, int64_t numel, float mu, void* stream);
+
+/*
+ * gns_muon_update: the last elementwise pass of muon_step on one tensor:
+ * W <- SR_bf16(decay*W - step*O), decay = 1 - lr*wd, step = lr*scale, all in
+ * fp32 with single roundings, SR keyed as in muon_step.
+ *   W_bf16 device bf16 bits [rows][cols], updated in place.
+ *   O_fp16 device fp16 bits [rows][cols], read.
+ */
+int gns_muon_update(uint16_t* W_bf16, const uint16_t* O_fp16, int rows, int cols, float lr,
+                    float wd, float scale, uint64_t seed, uint64_t step, int64_t base_index,
+                    void* stream);
+
+/*
+ * gns_symm_gemm: the symmetric product of Dion3 §5 (D = alpha A B + beta C
+ * with A B and C symmetric), batched over G matrices. Only lower-triangle
+ * tiles are computed; each is written to its own place and mirrored into the
+ * upper triangle, so D is exactly symmetric.
+ *   A  device fp16 [G][n][k] row-major.
+ *   B  device fp16 [G][n][k] row-major; the product is A B^T (the Gram
+ *      product X X^T when B == A; A B when B is symmetric and k == n).
+ *   C  device fp16 [G][n][n] (exactly symmetric) or NULL (beta ignored).
+ *   D  device fp16 [G][n][n], written.
+ * n and k must be multiples of 8 (16-byte rows). Asynchronous.
+ */
+int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, int n, int k,
+                  float alpha, float beta, void* stream);
+
+/* Synchronizes `stream`, returns the device status word of the current device
+ * as a gns_status (GNS_OK, GNS_ERR_NONFINITE or GNS_ERR_TIMEOUT) and clears it. */
+int gns_get_status(void* stream);
+
+/* Static text for a gns_status value. */
+const char* gns_status_string(int status);
+
+/* Text of the last failing CUDA call on this thread ("" if none). */
+const char* gns_last_error(void);
+
+/* Workspace bytes currently held on the current device. */
+int64_t gns_workspace_bytes(void);
+
+/* Frees the cached workspace of the current device (synchronizes it first). */
+void gns_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GNS_H */

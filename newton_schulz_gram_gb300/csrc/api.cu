@@ -1,0 +1,812 @@
+// C ABI, planner and workspace of the Gram Newton-Schulz library.
+//
+// The planner turns one bucket of G equal-shaped matrices into a fixed list
+// of grouped launches:
+//   sum of squares -> scale / cast / transpose (fp16 X and X^T) ->
+//   GEMM phases of Dion3 Algorithm 3 (or Algorithm 1 for square matrices).
+// Every GEMM phase covers all matrices of the bucket (or of a chunk of it),
+// so small matrices still fill the chip; per-tile arithmetic never depends on
+// G, so a matrix gives bit-identical results alone or inside a bucket.
+//
+// fp16 range: the fp16 copy is X~ = 2^k X (k = min(6, floor(log2 n) / 2)) and
+// every Gram-state matrix is carried as s = 4^k times its value (R~ = s R,
+// Z~ = s Z, RZ~ = s RZ; Q unscaled). The epilogue constants absorb the
+// scale exactly (powers of two): Z~ = b R~ + (c/s) R~R~,
+// Q' = (1/s) Q Z~ + a Q, RZ~ = (1/s) R~ Z~ + a R~, R~' = (1/s) Z~ RZ~ + a RZ~,
+// O = 2^-k Q X~. This keeps the entries of R (about 1/(n sqrt(m)) off the
+// diagonal at t = 0) out of the fp16 subnormal range.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "elementwise.cuh"
+#include "gemm.cuh"
+#include "gns.h"
+
+namespace gns {
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(GNS_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define CK(call)                                                        \
+    do {                                                                \
+        cudaError_t e_ = static_cast<cudaError_t>(call);                \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call);             \
+    } while (0)
+
+#define RET(call)                 \
+    do {                          \
+        int r_ = (call);          \
+        if (r_ != GNS_OK) return r_; \
+    } while (0)
+
+constexpr float kQuintic[3] = {3.4445f, -4.7750f, 2.0315f};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+long long round_up_ll(long long v, long long a) { return (v + a - 1) / a * a; }
+
+struct DeviceState {
+    int device = -1;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    char* ws = nullptr;
+    size_t ws_bytes = 0;
+    int* err = nullptr;
+    float* stage = nullptr;  // device staging for the host-buffer entry point
+    size_t stage_bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+
+int get_state(DeviceState** out) {
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (st.device < 0) {
+        CK(cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev));
+        CK(cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev));
+        CK(cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
+        st.device = dev;
+    }
+    if (!(st.cc_major == 10 && st.cc_minor == 3))
+        return fail(GNS_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300) only");
+    if (!st.err) {
+        CK(cudaMalloc(&st.err, 256));
+        CK(cudaMemset(st.err, 0, 256));
+    }
+    const char* cap = std::getenv("GNS_NUM_SMS");
+    if (cap && std::atoi(cap) > 0) st.num_sms = std::min(st.num_sms, std::atoi(cap));
+    *out = &st;
+    return GNS_OK;
+}
+
+int ensure_workspace(DeviceState& st, size_t bytes) {
+    if (st.ws_bytes >= bytes) return GNS_OK;
+    if (st.ws) {
+        CK(cudaDeviceSynchronize());
+        CK(cudaFree(st.ws));
+        st.ws = nullptr;
+        st.ws_bytes = 0;
+    }
+    const size_t want = align_up(bytes, size_t(2) << 20);
+    if (cudaMalloc(&st.ws, want) != cudaSuccess) {
+        cudaGetLastError();
+        st.ws = nullptr;
+        return fail(GNS_ERR_NOMEM, "workspace allocation of " + std::to_string(want) + " bytes failed");
+    }
+    st.ws_bytes = want;
+    return GNS_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A set of G row-major matrices in device memory.
+struct Mat {
+    void* p = nullptr;
+    int rows = 0, cols = 0;
+    long long ld = 0, stride = 0;
+    bool f32 = false;
+};
+
+int make_map(CUtensorMap* m, const Mat& x, int G, uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return fail(GNS_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const size_t es = x.f32 ? 4 : 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(x.cols), static_cast<cuuint64_t>(x.rows),
+                          static_cast<cuuint64_t>(G)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(x.ld) * es, static_cast<cuuint64_t>(x.stride) * es};
+    cuuint32_t box[3] = {box_c, box_r, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, x.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x.p, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[256];
+        std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (%d): %d x %d, ld %lld, G %d", static_cast<int>(r),
+                      x.rows, x.cols, x.ld, G);
+        return fail(GNS_ERR_INVALID, buf);
+    }
+    return GNS_OK;
+}
+
+// One problem of a phase: D = alpha A B^T (+ beta C) [, D2 = delta D + gamma I].
+struct ProblemSpec {
+    Mat A, B, D;
+    const Mat* C = nullptr;
+    const Mat* Dt = nullptr;
+    const Mat* D2 = nullptr;
+    const Mat* D2t = nullptr;
+    float alpha = 1.f, beta = 0.f, delta = 0.f, gamma = 0.f;
+    bool sym = false;
+};
+
+int set_problem(GemmProblem& pr, const ProblemSpec& sp, int G, int bn, int tile_begin) {
+    std::memset(&pr, 0, sizeof(pr));
+    if (sp.A.cols != sp.B.cols) return fail(GNS_ERR_INVALID, "operand K mismatch");
+    if ((sp.sym || sp.D2) && bn != 128) return fail(GNS_ERR_INVALID, "symmetric/second-output phases need 128-wide tiles");
+    if (sp.sym && sp.A.rows != sp.B.rows) return fail(GNS_ERR_INVALID, "symmetric product must be square");
+    if (sp.D2 && sp.Dt && !sp.D2t) return fail(GNS_ERR_INVALID, "second output needs its transposed map");
+    if (sp.D.f32 && (sp.Dt || sp.D2)) return fail(GNS_ERR_INVALID, "fp32 output supports no transposed/second output");
+    if (G > 65535) return fail(GNS_ERR_INVALID, "too many matrices in one launch");
+    RET(make_map(&pr.tmA, sp.A, G, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    RET(make_map(&pr.tmB, sp.B, G, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B));
+    RET(make_map(&pr.tmD, sp.D, G, 32, 32, sp.D.f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B));
+    int flags = 0;
+    if (sp.sym) flags |= kFlagSym;
+    if (sp.D.f32) flags |= kFlagOutF32;
+    if (sp.C) {
+        flags |= kFlagC;
+        pr.C = static_cast<const __half*>(sp.C->p);
+        pr.ldc = sp.C->ld;
+        pr.strideC = sp.C->stride;
+    }
+    if (sp.Dt) {
+        flags |= kFlagDt;
+        RET(make_map(&pr.tmDt, *sp.Dt, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
+    }
+    if (sp.D2) {
+        flags |= kFlagD2;
+        RET(make_map(&pr.tmD2, *sp.D2, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
+        if (sp.D2t) RET(make_map(&pr.tmD2t, *sp.D2t, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
+    }
+    pr.alpha = sp.alpha;
+    pr.beta = sp.beta;
+    pr.delta = sp.delta;
+    pr.gamma = sp.gamma;
+    pr.M = sp.A.rows;
+    pr.N = sp.B.rows;
+    pr.K = sp.A.cols;
+    pr.G = G;
+    pr.tiles_m = (pr.M + 127) / 128;
+    pr.tiles_n = (pr.N + bn - 1) / bn;
+    pr.tiles_per_matrix = sp.sym ? pr.tiles_m * (pr.tiles_m + 1) / 2 : pr.tiles_m * pr.tiles_n;
+    pr.tile_begin = tile_begin;
+    pr.flags = flags;
+    return GNS_OK;
+}
+
+int run_phase(DeviceState& st, int G, int bn, const ProblemSpec& p0, const ProblemSpec* p1, cudaStream_t s) {
+    GemmPhase ph;
+    std::memset(&ph, 0, sizeof(ph));
+    RET(set_problem(ph.prob[0], p0, G, bn, 0));
+    ph.nprob = 1;
+    int total = ph.prob[0].tiles_per_matrix * G;
+    if (p1) {
+        RET(set_problem(ph.prob[1], *p1, G, bn, total));
+        ph.nprob = 2;
+        total += ph.prob[1].tiles_per_matrix * G;
+    }
+    ph.total_tiles = total;
+    ph.err = st.err;
+    CK(launch_gemm_phase(ph, bn, st.num_sms, s));
+    return GNS_OK;
+}
+
+// --------------------------------------------------------------- planner
+
+int ilog2(int v) {
+    int r = 0;
+    while ((1 << (r + 1)) <= v) ++r;
+    return r;
+}
+
+struct Coeffs {
+    std::vector<float> a, b, c;
+};
+
+int load_coeffs(const float* coeffs, int steps, Coeffs& out) {
+    out.a.resize(steps);
+    out.b.resize(steps);
+    out.c.resize(steps);
+    for (int t = 0; t < steps; ++t) {
+        const float* src = coeffs ? coeffs + 3 * t : kQuintic;
+        if (!std::isfinite(src[0]) || !std::isfinite(src[1]) || !std::isfinite(src[2]))
+            return fail(GNS_ERR_INVALID, "non-finite coefficient");
+        out.a[t] = src[0];
+        out.b[t] = src[1];
+        out.c[t] = src[2];
+    }
+    return GNS_OK;
+}
+
+bool is_restart_after(int t, int steps, int restart_at) {
+    return restart_at > 0 && t >= 1 && t < steps && t % restart_at == 0 && steps - t >= restart_at;
+}
+
+// Where the result of one bucket goes.
+struct OutSpec {
+    Mat out;        // fp32 [G][R][C] (ABI) or fp16 [G][R][ld] (Muon O)
+    bool copy_back = false;  // out is a workspace buffer; copy to user_ptr afterwards
+    float* user_ptr = nullptr;
+};
+
+struct BucketGeom {
+    int R, C, n, m;
+    bool transposed, square;
+    long long ldn, ldm;
+    int k_exp;
+    float s;  // 4^k
+};
+
+BucketGeom make_geom(int R, int C) {
+    BucketGeom g;
+    g.R = R;
+    g.C = C;
+    g.n = std::min(R, C);
+    g.m = std::max(R, C);
+    g.transposed = R > C;
+    g.square = R == C;
+    g.ldn = round_up_ll(g.n, 8);
+    g.ldm = round_up_ll(g.m, 8);
+    g.k_exp = std::min(6, ilog2(g.n) / 2);
+    g.s = std::ldexp(1.0f, 2 * g.k_exp);
+    return g;
+}
+
+// Workspace layout for a chunk of Gc matrices.
+struct Layout {
+    size_t xa, xta, xb, xtb, r, z, rz, qa, qb, partial, out32, o16, meta, total;
+    long long ld_out32;
+};
+
+Layout make_layout(const BucketGeom& g, int Gc, bool need_out32, bool need_o16, size_t meta_bytes) {
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    const size_t nm = static_cast<size_t>(g.n) * g.ldm * 2 * Gc;    // X: n x m
+    const size_t mn = static_cast<size_t>(g.m) * g.ldn * 2 * Gc;    // X^T: m x n
+    const size_t nn = static_cast<size_t>(g.n) * g.ldn * 2 * Gc;
+    L.xa = take(nm);
+    L.xta = take(mn);
+    L.xb = g.square ? take(nm) : 0;
+    L.xtb = take(mn);
+    L.r = take(nn);
+    L.z = take(nn);
+    L.rz = g.square ? 0 : take(nn);
+    L.qa = g.square ? 0 : take(nn);
+    L.qb = g.square ? 0 : take(nn);
+    L.partial = take(static_cast<size_t>(Gc) * 64 * 4);
+    L.ld_out32 = round_up_ll(g.C, 4);
+    L.out32 = need_out32 ? take(static_cast<size_t>(g.R) * L.ld_out32 * 4 * Gc) : 0;
+    L.o16 = need_o16 ? take(static_cast<size_t>(g.R) * round_up_ll(g.C, 8) * 2 * Gc) : 0;
+    L.meta = take(meta_bytes);
+    L.total = off;
+    return L;
+}
+
+Mat mat16(char* ws, size_t off, int rows, int cols, long long ld) {
+    Mat m;
+    m.p = ws + off;
+    m.rows = rows;
+    m.cols = cols;
+    m.ld = ld;
+    m.stride = static_cast<long long>(rows) * ld;
+    m.f32 = false;
+    return m;
+}
+
+// Runs the orthogonalization of one chunk of Gc matrices whose sum-of-squares
+// partials are already in L.partial (nblk per matrix).
+int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in, int nblk, int steps,
+             int restart_at, const Coeffs& cf, const OutSpec& os, cudaStream_t s) {
+    char* ws = st.ws;
+    const int n = g.n, m = g.m;
+    Mat Xa = mat16(ws, L.xa, n, m, g.ldm);
+    Mat XTa = mat16(ws, L.xta, m, n, g.ldn);
+    Mat XTb = mat16(ws, L.xtb, m, n, g.ldn);
+    // Scale + cast: the input (R x C) is written directly and transposed.
+    {
+        const Mat& direct = g.transposed ? XTa : Xa;
+        const Mat& trans = g.transposed ? Xa : XTa;
+        CK(launch_scale_cast(in, Gc, g.R, g.C, reinterpret_cast<const float*>(ws + L.partial), nblk, g.k_exp,
+                             direct.p, direct.ld, direct.stride, trans.p, trans.ld, trans.stride, st.err, s));
+    }
+    const float inv_s = 1.0f / g.s;
+    const float out_scale = std::ldexp(1.0f, -g.k_exp);
+
+    if (g.square) {
+        // Dion3 Algorithm 1 with symmetric A = X X^T and B = b A + c A^2
+        // (App. C.3): X <- a X + B X, the last step writing the output.
+        Mat Xb = mat16(ws, L.xb, n, n, g.ldn);
+        Mat A = mat16(ws, L.r, n, n, g.ldn);
+        Mat B = mat16(ws, L.z, n, n, g.ldn);
+        Mat X = Xa, XT = XTa, Xn = Xb, XTn = XTb;
+        for (int t = 0; t < steps; ++t) {
+            ProblemSpec pa;
+            pa.A = X;
+            pa.B = X;
+            pa.D = A;
+            pa.Dt = &A;
+            pa.sym = true;
+            RET(run_phase(st, Gc, 128, pa, nullptr, s));
+            ProblemSpec pb;
+            pb.A = A;
+            pb.B = A;
+            pb.C = &A;
+            pb.D = B;
+            pb.Dt = &B;
+            pb.alpha = cf.c[t] * inv_s;
+            pb.beta = cf.b[t];
+            pb.sym = true;
+            RET(run_phase(st, Gc, 128, pb, nullptr, s));
+            ProblemSpec px;
+            px.A = B;
+            px.B = XT;
+            px.C = &X;
+            if (t + 1 < steps) {
+                px.D = Xn;
+                px.Dt = &XTn;
+                px.alpha = inv_s;
+                px.beta = cf.a[t];
+                RET(run_phase(st, Gc, 256, px, nullptr, s));
+                std::swap(X, Xn);
+                std::swap(XT, XTn);
+            } else {
+                px.D = os.out;
+                px.alpha = inv_s * out_scale;
+                px.beta = cf.a[t] * out_scale;
+                RET(run_phase(st, Gc, 256, px, nullptr, s));
+            }
+        }
+        return GNS_OK;
+    }
+
+    // Dion3 Algorithm 3 with the App. B.2.3 a-term distribution.
+    Mat R = mat16(ws, L.r, n, n, g.ldn);
+    Mat Z = mat16(ws, L.z, n, n, g.ldn);
+    Mat RZ = mat16(ws, L.rz, n, n, g.ldn);
+    Mat Qc = mat16(ws, L.qa, n, n, g.ldn);
+    Mat Qn = mat16(ws, L.qb, n, n, g.ldn);
+    Mat X = Xa, XT = XTa, XTn = XTb;
+
+    auto gram = [&](void) -> int {
+        ProblemSpec p;
+        p.A = X;
+        p.B = X;
+        p.D = R;
+        p.Dt = &R;
+        p.sym = true;
+        return run_phase(st, Gc, 128, p, nullptr, s);
+    };
+    RET(gram());
+    bool q_identity = true;
+    for (int t = 1; t <= steps; ++t) {
+        const float a = cf.a[t - 1], b = cf.b[t - 1], c = cf.c[t - 1];
+        if (is_restart_after(t - 1, steps, restart_at)) {
+            // X <- Q X (n x m) and its transpose, then R <- X X^T, Q <- I.
+            ProblemSpec p;
+            p.A = Qc;
+            p.B = XT;
+            p.D = X;  // X is not read by this phase
+            p.Dt = &XTn;
+            RET(run_phase(st, Gc, 256, p, nullptr, s));
+            std::swap(XT, XTn);
+            RET(gram());
+            q_identity = true;
+        }
+        const bool need_r = t < steps && !is_restart_after(t, steps, restart_at);
+        // Z = b R + c R^2 (with Q = Z + a I written alongside after a (re)start).
+        {
+            ProblemSpec p;
+            p.A = R;
+            p.B = R;
+            p.C = &R;
+            p.D = Z;
+            p.Dt = &Z;
+            p.alpha = c * inv_s;
+            p.beta = b;
+            p.sym = true;
+            if (q_identity) {
+                p.D2 = &Qc;
+                p.D2t = &Qc;
+                p.delta = inv_s;
+                p.gamma = a;
+            }
+            RET(run_phase(st, Gc, 128, p, nullptr, s));
+        }
+        ProblemSpec pq, prz;
+        if (!q_identity) {
+            pq.A = Qc;
+            pq.B = Z;
+            pq.C = &Qc;
+            pq.D = Qn;
+            pq.Dt = &Qn;
+            pq.alpha = inv_s;
+            pq.beta = a;
+            pq.sym = true;
+        }
+        if (need_r) {
+            prz.A = R;
+            prz.B = Z;
+            prz.C = &R;
+            prz.D = RZ;
+            prz.Dt = &RZ;
+            prz.alpha = inv_s;
+            prz.beta = a;
+            prz.sym = true;
+        }
+        if (!q_identity && need_r) {
+            RET(run_phase(st, Gc, 128, pq, &prz, s));
+        } else if (!q_identity) {
+            RET(run_phase(st, Gc, 128, pq, nullptr, s));
+        } else if (need_r) {
+            RET(run_phase(st, Gc, 128, prz, nullptr, s));
+        }
+        if (!q_identity) std::swap(Qc, Qn);
+        q_identity = false;
+        if (need_r) {
+            ProblemSpec p;
+            p.A = Z;
+            p.B = RZ;
+            p.C = &RZ;
+            p.D = R;
+            p.Dt = &R;
+            p.alpha = inv_s;
+            p.beta = a;
+            p.sym = true;
+            RET(run_phase(st, Gc, 128, p, nullptr, s));
+        }
+    }
+    // O = Q X, written in the caller's orientation.
+    ProblemSpec p;
+    if (!g.transposed) {
+        p.A = Qc;
+        p.B = XT;
+    } else {
+        p.A = XT;
+        p.B = Qc;
+    }
+    p.D = os.out;
+    p.alpha = out_scale;
+    RET(run_phase(st, Gc, 256, p, nullptr, s));
+    return GNS_OK;
+}
+
+size_t chunk_cap_bytes() {
+    const char* e = std::getenv("GNS_WORKSPACE_CAP_MB");
+    if (e && std::atoll(e) > 0) return static_cast<size_t>(std::atoll(e)) << 20;
+    return size_t(24) << 30;
+}
+
+int validate_common(int G, int R, int C, int steps) {
+    if (G < 0 || R < 1 || C < 1) return fail(GNS_ERR_INVALID, "G must be >= 0 and R, C >= 1");
+    if (steps < 1 || steps > GNS_MAX_STEPS) return fail(GNS_ERR_INVALID, "steps must be in 1..GNS_MAX_STEPS");
+    if (static_cast<long long>(R) * C > (1LL << 40)) return fail(GNS_ERR_INVALID, "matrix too large");
+    return GNS_OK;
+}
+
+int chunk_size(const BucketGeom& g, int G, bool out32, bool o16) {
+    const Layout one = make_layout(g, 1, out32, o16, 0);
+    size_t per = one.total;
+    size_t cap = chunk_cap_bytes();
+    long long c = static_cast<long long>(cap / std::max<size_t>(per, 1));
+    if (c < 1) c = 1;
+    if (c > G) c = G;
+    if (c > 65535) c = 65535;
+    return static_cast<int>(c);
+}
+
+int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart_at, const float* coeffs,
+                         cudaStream_t s) {
+    RET(validate_common(G, R, C, steps));
+    if (G == 0) return GNS_OK;
+    if (!ptr) return fail(GNS_ERR_INVALID, "ptr is null");
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    Coeffs cf;
+    RET(load_coeffs(coeffs, steps, cf));
+    const BucketGeom g = make_geom(R, C);
+    const bool direct_out = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && ((static_cast<long long>(C) * 4) % 16 == 0);
+    const int Gc = chunk_size(g, G, !direct_out, false);
+    const Layout L = make_layout(g, Gc, !direct_out, false, 0);
+    RET(ensure_workspace(*st, L.total));
+    const long long numel = static_cast<long long>(R) * C;
+    const int nblk = norm_blocks(numel);
+    for (int g0 = 0; g0 < G; g0 += Gc) {
+        const int gc = std::min(Gc, G - g0);
+        float* base = ptr + static_cast<long long>(g0) * numel;
+        MatrixSet in{base, numel, nullptr};
+        CK(launch_sumsq(in, numel, gc, reinterpret_cast<float*>(st->ws + L.partial), st->err, s));
+        OutSpec os;
+        if (direct_out) {
+            os.out.p = base;
+            os.out.rows = R;
+            os.out.cols = C;
+            os.out.ld = C;
+            os.out.stride = numel;
+            os.out.f32 = true;
+        } else {
+            os.out.p = st->ws + L.out32;
+            os.out.rows = R;
+            os.out.cols = C;
+            os.out.ld = L.ld_out32;
+            os.out.stride = static_cast<long long>(R) * L.ld_out32;
+            os.out.f32 = true;
+        }
+        RET(run_core(*st, g, L, gc, in, nblk, steps, restart_at, cf, os, s));
+        if (!direct_out)
+            CK(launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
+    }
+    return GNS_OK;
+}
+
+}  // namespace
+}  // namespace gns
+
+using namespace gns;
+
+extern "C" {
+
+int gns_orthogonalize_batched(float* ptr, int G, int R, int C, int steps, int restart_at, const float* coeffs,
+                              void* stream) {
+    return orthogonalize_device(ptr, G, R, C, steps, restart_at, coeffs, static_cast<cudaStream_t>(stream));
+}
+
+int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int steps, int restart_at,
+                                   const float* coeffs, void* stream) {
+    RET(validate_common(G, R, C, steps));
+    if (G == 0) return GNS_OK;
+    if (!host_ptr) return fail(GNS_ERR_INVALID, "host_ptr is null");
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = static_cast<size_t>(G) * R * C * sizeof(float);
+    if (st->stage_bytes < bytes) {
+        if (st->stage) {
+            CK(cudaDeviceSynchronize());
+            CK(cudaFree(st->stage));
+            st->stage = nullptr;
+            st->stage_bytes = 0;
+        }
+        if (cudaMalloc(&st->stage, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(GNS_ERR_NOMEM, "staging allocation failed");
+        }
+        st->stage_bytes = bytes;
+    }
+    CK(cudaMemcpyAsync(st->stage, host_ptr, bytes, cudaMemcpyHostToDevice, s));
+    RET(orthogonalize_device(st->stage, G, R, C, steps, restart_at, coeffs, s));
+    CK(cudaMemcpyAsync(host_ptr, st->stage, bytes, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    return GNS_OK;
+}
+
+int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n, float lr,
+              float wd, float mu, uint64_t seed, uint64_t step, void* stream) {
+    if (n < 0) return fail(GNS_ERR_INVALID, "n < 0");
+    if (n == 0) return GNS_OK;
+    if (!params || !grads || !momentum) return fail(GNS_ERR_INVALID, "null tensor array");
+    for (int i = 0; i < n; ++i) {
+        const gns_tensor &w = params[i], &gr = grads[i], &mm = momentum[i];
+        if (!w.data || !gr.data || !mm.data) return fail(GNS_ERR_INVALID, "null tensor data");
+        if (w.rows < 1 || w.cols < 1 || gr.rows != w.rows || gr.cols != w.cols || mm.rows != w.rows ||
+            mm.cols != w.cols)
+            return fail(GNS_ERR_INVALID, "tensor shapes differ");
+        if (w.base_index < 0) return fail(GNS_ERR_INVALID, "negative base_index");
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    // Buckets of equal (rows, cols), in order of first appearance.
+    std::vector<std::pair<std::pair<int, int>, std::vector<int>>> buckets;
+    for (int i = 0; i < n; ++i) {
+        auto key = std::make_pair(params[i].rows, params[i].cols);
+        auto it = std::find_if(buckets.begin(), buckets.end(), [&](const auto& b) { return b.first == key; });
+        if (it == buckets.end()) {
+            buckets.push_back({key, {i}});
+        } else {
+            it->second.push_back(i);
+        }
+    }
+    Coeffs cf;
+    RET(load_coeffs(nullptr, 5, cf));
+    for (auto& bk : buckets) {
+        const int R = bk.first.first, C = bk.first.second;
+        const int G = static_cast<int>(bk.second.size());
+        const BucketGeom g = make_geom(R, C);
+        const int Gc = chunk_size(g, G, false, true);
+        const size_t meta_bytes = static_cast<size_t>(Gc) * (3 * sizeof(void*) + sizeof(long long)) + 256;
+        const Layout L = make_layout(g, Gc, false, true, meta_bytes);
+        RET(ensure_workspace(*st, L.total));
+        const long long numel = static_cast<long long>(R) * C;
+        const long long ld_o = round_up_ll(C, 8);
+        const float scale = 0.2f * std::sqrt(static_cast<float>(std::max(R, C)));
+        for (int g0 = 0; g0 < G; g0 += Gc) {
+            const int gc = std::min(Gc, G - g0);
+            std::vector<const void*> ptrs(3 * static_cast<size_t>(gc));
+            std::vector<long long> bases(gc);
+            for (int j = 0; j < gc; ++j) {
+                const int i = bk.second[g0 + j];
+                ptrs[j] = momentum[i].data;
+                ptrs[gc + j] = grads[i].data;
+                ptrs[2 * gc + j] = params[i].data;
+                bases[j] = params[i].base_index;
+            }
+            char* meta = st->ws + L.meta;
+            CK(cudaMemcpyAsync(meta, ptrs.data(), ptrs.size() * sizeof(void*), cudaMemcpyHostToDevice, s));
+            long long* bases_dev = reinterpret_cast<long long*>(meta + align_up(ptrs.size() * sizeof(void*), 16));
+            CK(cudaMemcpyAsync(bases_dev, bases.data(), bases.size() * sizeof(long long), cudaMemcpyHostToDevice, s));
+            const void* const* pm = reinterpret_cast<const void* const*>(meta);
+            MatrixSet Ms{nullptr, 0, pm};
+            MatrixSet Gs{nullptr, 0, pm + gc};
+            MatrixSet Ws{nullptr, 0, pm + 2 * gc};
+            float* partial = reinterpret_cast<float*>(st->ws + L.partial);
+            CK(launch_momentum(Ms, Gs, numel, gc, mu, partial, s));
+            OutSpec os;
+            os.out.p = st->ws + L.o16;
+            os.out.rows = R;
+            os.out.cols = C;
+            os.out.ld = ld_o;
+            os.out.stride = static_cast<long long>(R) * ld_o;
+            os.out.f32 = false;
+            RET(run_core(*st, g, L, gc, Ms, norm_blocks(numel), 5, 2, cf, os, s));
+            MatrixSet Os{os.out.p, os.out.stride, nullptr};
+            CK(launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s));
+        }
+    }
+    return GNS_OK;
+}
+
+int gns_muon_momentum(float* M, const uint16_t* G_bf16, int64_t numel, float mu, void* stream) {
+    if (numel < 0 || (numel > 0 && (!M || !G_bf16))) return fail(GNS_ERR_INVALID, "bad momentum arguments");
+    if (numel == 0) return GNS_OK;
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    MatrixSet Ms{M, numel, nullptr};
+    MatrixSet Gs{G_bf16, numel, nullptr};
+    CK(launch_momentum(Ms, Gs, numel, 1, mu, nullptr, static_cast<cudaStream_t>(stream)));
+    return GNS_OK;
+}
+
+int gns_muon_update(uint16_t* W_bf16, const uint16_t* O_fp16, int rows, int cols, float lr, float wd, float scale,
+                    uint64_t seed, uint64_t step, int64_t base_index, void* stream) {
+    if (rows < 0 || cols < 0 || base_index < 0) return fail(GNS_ERR_INVALID, "bad update arguments");
+    if (static_cast<long long>(rows) * cols == 0) return GNS_OK;
+    if (!W_bf16 || !O_fp16) return fail(GNS_ERR_INVALID, "null pointer");
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    const long long numel = static_cast<long long>(rows) * cols;
+    MatrixSet Ws{W_bf16, numel, nullptr};
+    MatrixSet Os{O_fp16, numel, nullptr};
+    CK(launch_muon_update(Ws, Os, cols, nullptr, base_index, 1, rows, cols, lr, wd, scale, seed, step,
+                          static_cast<cudaStream_t>(stream)));
+    return GNS_OK;
+}
+
+int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, int n, int k, float alpha, float beta,
+                  void* stream) {
+    if (G < 0 || n < 1 || k < 1) return fail(GNS_ERR_INVALID, "G >= 0, n >= 1 and k >= 1 required");
+    if (G == 0) return GNS_OK;
+    if (!A || !B || !D) return fail(GNS_ERR_INVALID, "null pointer");
+    if (n % 8 || k % 8) return fail(GNS_ERR_INVALID, "n and k must be multiples of 8");
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    Mat a{const_cast<void*>(A), n, k, k, static_cast<long long>(n) * k, false};
+    Mat b{const_cast<void*>(B), n, k, k, static_cast<long long>(n) * k, false};
+    Mat d{D, n, n, n, static_cast<long long>(n) * n, false};
+    Mat c{const_cast<void*>(C), n, n, n, static_cast<long long>(n) * n, false};
+    ProblemSpec p;
+    p.A = a;
+    p.B = b;
+    p.D = d;
+    p.Dt = &d;
+    p.C = C ? &c : nullptr;
+    p.alpha = alpha;
+    p.beta = C ? beta : 0.0f;
+    p.sym = true;
+    return run_phase(*st, G, 128, p, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int gns_get_status(void* stream) {
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    int v = 0;
+    CK(cudaMemcpy(&v, st->err, sizeof(int), cudaMemcpyDeviceToHost));
+    CK(cudaMemset(st->err, 0, sizeof(int)));
+    return v;
+}
+
+const char* gns_status_string(int status) {
+    switch (status) {
+        case GNS_OK: return "ok";
+        case GNS_ERR_INVALID: return "invalid argument";
+        case GNS_ERR_CUDA: return "CUDA runtime error";
+        case GNS_ERR_NONFINITE: return "non-finite input norm";
+        case GNS_ERR_TIMEOUT: return "device wait timed out";
+        case GNS_ERR_NOMEM: return "out of device memory";
+        case GNS_ERR_UNSUPPORTED: return "unsupported device (sm_103a required)";
+        default: return "unknown status";
+    }
+}
+
+const char* gns_last_error(void) { return g_last_error.c_str(); }
+
+int64_t gns_workspace_bytes(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(dev);
+    return it == g_dev.end() ? 0 : static_cast<int64_t>(it->second.ws_bytes);
+}
+
+void gns_release(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(dev);
+    if (it == g_dev.end()) return;
+    cudaDeviceSynchronize();
+    if (it->second.ws) cudaFree(it->second.ws);
+    if (it->second.stage) cudaFree(it->second.stage);
+    it->second.ws = nullptr;
+    it->second.ws_bytes = 0;
+    it->second.stage = nullptr;
+    it->second.stage_bytes = 0;
+}
+
+}  // extern "C"

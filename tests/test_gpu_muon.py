@@ -1,0 +1,121 @@
+"""Muon elementwise passes and the full Muon step on the GPU, through the C
+ABI, against the CPU oracle (bitwise where the arithmetic is fixed)."""
+import numpy as np
+import pytest
+
+from gpu_helpers import assert_parity
+from inputs import generators as gen
+from oracle import gram_ns as O
+from oracle import muon as MU
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gns():
+    import newton_schulz_gram_gb300 as m
+    from newton_schulz_gram_gb300 import build
+    build.build()
+    m.load()
+    return m
+
+
+def bf16_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_momentum_bitwise(gns):
+    for numel in (1, 7, 4096, 100003):
+        rng = np.random.default_rng(numel)
+        M = rng.standard_normal(numel).astype(np.float32)
+        Gv = (1e-3 * rng.standard_normal(numel)).astype(np.float32)
+        Gb = torch.from_numpy(Gv).to(torch.bfloat16)
+        tM = torch.from_numpy(M).cuda()
+        gns.gns_muon_momentum(tM, Gb.cuda(), 0.95)
+        want = MU.momentum(M, Gb.float().numpy(), 0.95)
+        assert np.array_equal(tM.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("rows,cols,base", [(64, 256, 0), (33, 45, 0), (128, 128, 6), (7, 9, 1001), (256, 1024, 1 << 33)])
+def test_update_bitwise(gns, rows, cols, base):
+    rng = np.random.default_rng(rows * cols + base)
+    w = (0.02 * rng.standard_normal((rows, cols))).astype(np.float32)
+    o = (rng.standard_normal((rows, cols)) / np.sqrt(cols)).astype(np.float16)
+    W = torch.from_numpy(w).to(torch.bfloat16)
+    w_bits = bf16_bits(W)
+    tW = W.cuda()
+    lr, wd, scale, seed, step = 0.02, 0.01, float(MU.update_scale(rows, cols)), 1234567890123, 17
+    gns.gns_muon_update(tW, torch.from_numpy(o).cuda(), lr, wd, scale, seed, step, base)
+    want = MU.muon_update_bf16(w_bits, o.astype(np.float32), lr, wd, np.float32(scale), seed, step, base)
+    assert np.array_equal(bf16_bits(tW), want)
+
+
+def test_update_shards_match_whole(gns):
+    rows, cols = 64, 512
+    rng = np.random.default_rng(3)
+    W = torch.from_numpy((0.02 * rng.standard_normal((rows, cols))).astype(np.float32)).to(torch.bfloat16).cuda()
+    O16 = torch.from_numpy((rng.standard_normal((rows, cols)) / 20).astype(np.float16)).cuda()
+    whole = W.clone()
+    gns.gns_muon_update(whole, O16, 0.02, 0.01, 2.0, 5, 6, 1000)
+    top, bot = W[:24].clone(), W[24:].clone()
+    gns.gns_muon_update(top, O16[:24].contiguous(), 0.02, 0.01, 2.0, 5, 6, 1000)
+    gns.gns_muon_update(bot, O16[24:].contiguous(), 0.02, 0.01, 2.0, 5, 6, 1000 + 24 * cols)
+    assert torch.equal(torch.cat([top, bot]), whole)
+
+
+@pytest.mark.parametrize("p", [0.1, 0.25, 0.5])
+def test_sr_unbiased_on_gpu(gns, p):
+    """Muon kernel card: a sub-ULP update over 2e5 bf16 elements averages to
+    the true value. W = 1 + p ULP is built as (1 - lr wd) W - lr s O with
+    W = 1, wd = 0, lr s O = -p ULP exactly."""
+    n = 200_000
+    ulp = 2.0 ** -7
+    errs = []
+    for k in range(16):
+        W = torch.ones(1, n, dtype=torch.bfloat16, device="cuda")
+        # o = -p * ulp / (lr * scale) with lr = 1, scale = 2^-10: fp16-exact for p in {0.1 (rounded), 0.25, 0.5}
+        o = torch.full((1, n), -p * ulp * 1024.0, dtype=torch.float16, device="cuda")
+        # The fp32 value the kernel rounds: 1 - fl(2^-10 * o), each step exact or rounded once.
+        target = float(np.float32(1.0) - np.float32(2.0 ** -10) * np.float32(o[0, 0].item()))
+        gns.gns_muon_update(W, o, 1.0, 0.0, 2.0 ** -10, 100 + k, k, 0)
+        errs.append((W.float().double().mean().item() - target) / ulp)
+    assert abs(np.mean(errs)) < 1e-3
+
+
+def test_muon_step_matches_oracle(gns):
+    shapes = [(128, 512), (512, 128), (128, 512), (256, 256), (96, 200)]
+    rng_seed = 21
+    Ws, Gs, Ms = [], [], []
+    for i, (r, c) in enumerate(shapes):
+        w, g = gen.muon_param_inputs(r, c, seed=rng_seed, index=i)
+        Ws.append(torch.from_numpy(w).to(torch.bfloat16))
+        Gs.append(torch.from_numpy(g).to(torch.bfloat16))
+        Ms.append(torch.from_numpy(np.random.default_rng(i).standard_normal((r, c)).astype(np.float32) * 1e-3))
+    w_bits = [bf16_bits(w) for w in Ws]
+    g_bits = [bf16_bits(g) for g in Gs]
+    m_np = [m.numpy().copy() for m in Ms]
+    dW = [w.cuda() for w in Ws]
+    dG = [g.cuda() for g in Gs]
+    dM = [m.cuda() for m in Ms]
+    bases = [1000 * i for i in range(len(shapes))]
+    gns.muon_step(dW, dG, dM, lr=0.02, wd=0.01, mu=0.95, seed=0, step=3, base_indices=bases)
+    torch.cuda.synchronize()
+    assert gns.gns_get_status() == 0
+    new_w, new_m, outs = MU.muon_step(w_bits, g_bits, m_np, 0.02, 0.01, 0.95, 0, 3, bases)
+    for i, (r, c) in enumerate(shapes):
+        assert np.array_equal(dM[i].cpu().numpy(), new_m[i]), f"momentum {i}"
+        w_old = MU.bf16_bits_to_f32(w_bits[i]).astype(np.float64)
+        got_delta = MU.bf16_bits_to_f32(bf16_bits(dW[i])).astype(np.float64) - w_old
+        want_delta = MU.bf16_bits_to_f32(new_w[i]).astype(np.float64) - w_old
+        # The update direction is the orthogonalized momentum: compare the
+        # updates themselves. Each side's stochastic rounding adds at most one
+        # bf16 ULP of |w| per element.
+        ulp = np.abs(w_old) * 2.0 ** -7
+        s = float(MU.update_scale(r, c))
+        step = 0.02 * s * outs[i]
+        noise = np.linalg.norm(ulp) * 2
+        rel = np.linalg.norm(got_delta - want_delta) / np.linalg.norm(want_delta)
+        bound = 3e-2 + noise / np.linalg.norm(want_delta)
+        assert rel <= bound, (i, rel, bound)
+        assert np.linalg.norm(want_delta + step + 0.02 * 0.01 * w_old) <= noise
