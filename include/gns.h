@@ -159,6 +159,22 @@ const char* gns_status_string(int status);
 /* Text of the last failing CUDA call on this thread ("" if none). */
 const char* gns_last_error(void);
 
+/* Number of kernel launches the library has issued since it was loaded
+ * (all devices, all entry points). */
+int64_t gns_launch_count(void);
+
+/* Measurement support. With profiling on (on != 0), every kernel launch is
+ * bracketed by two CUDA events recorded on its own stream. Off by default. */
+void gns_profile_enable(int on);
+
+/* Synchronizes the recorded events and returns, per kernel class, the number
+ * of profiled launches (counts[k]) and their summed event durations in ms
+ * (ms[k]) since the previous read; then forgets them. Classes: 0 tcgen05
+ * GEMM, 1 norm (sum of squares), 2 scale/cast/transpose, 3 Muon elementwise,
+ * 4 output copy. Writes min(max_classes, 5) entries of each non-null array
+ * and returns the number of classes (5), or a negative gns_status. */
+int gns_profile_read(int64_t* counts, double* ms, int max_classes);
+
 /* Workspace bytes currently held on the current device. */
 int64_t gns_workspace_bytes(void);
 

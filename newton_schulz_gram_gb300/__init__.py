@@ -16,6 +16,7 @@ from ._lib import GnsError, GnsTensor, check, load
 __all__ = ["gns_orthogonalize_batched", "gns_orthogonalize_batched_host", "muon_step",
            "gns_muon_momentum", "gns_muon_update", "gns_symm_gemm", "gns_get_status",
            "gns_status_string", "gns_last_error", "gns_workspace_bytes", "gns_release",
+           "gns_launch_count", "gns_profile_enable", "gns_profile_read", "KERNEL_CLASSES",
            "GnsError", "QUINTIC", "load"]
 
 QUINTIC = (3.4445, -4.7750, 2.0315)
@@ -158,6 +159,27 @@ def gns_status_string(status):
 
 def gns_last_error():
     return load().gns_last_error().decode(errors="replace")
+
+
+KERNEL_CLASSES = ("gemm_tc", "sumsq", "scale_cast", "muon_elementwise", "copy_rows")
+
+
+def gns_launch_count():
+    """Kernel launches issued by the library since it was loaded."""
+    return load().gns_launch_count()
+
+
+def gns_profile_enable(on=True):
+    load().gns_profile_enable(1 if on else 0)
+
+
+def gns_profile_read():
+    """{class: (launches, total ms)} of the profiled launches since the last read."""
+    n = len(KERNEL_CLASSES)
+    counts = (ctypes.c_int64 * n)()
+    ms = (ctypes.c_double * n)()
+    check(min(0, load().gns_profile_read(counts, ms, n)), "gns_profile_read")
+    return {k: (counts[i], ms[i]) for i, k in enumerate(KERNEL_CLASSES)}
 
 
 def gns_workspace_bytes():

@@ -34,6 +34,9 @@ PROTOTYPES = {
     "gns_status_string": (ctypes.c_char_p, [_i]),
     "gns_last_error": (ctypes.c_char_p, []),
     "gns_workspace_bytes": (_i64, []),
+    "gns_launch_count": (_i64, []),
+    "gns_profile_enable": (None, [_i]),
+    "gns_profile_read": (_i, [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double), _i]),
     "gns_release": (None, []),
 }
 

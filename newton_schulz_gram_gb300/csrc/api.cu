@@ -24,6 +24,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -118,6 +119,60 @@ int ensure_workspace(DeviceState& st, size_t bytes) {
     st.ws_bytes = want;
     return GNS_OK;
 }
+
+// ------------------------------------------------------- launch accounting
+//
+// Every kernel launch is counted. When profiling is on, each launch is also
+// bracketed by a pair of CUDA events on its own stream; gns_profile_read()
+// turns them into per-class launch counts and summed durations.
+
+enum KernelClass { kClsGemm = 0, kClsNorm = 1, kClsCast = 2, kClsMuon = 3, kClsCopy = 4, kNumCls = 5 };
+
+std::atomic<long long> g_launches{0};
+std::atomic<bool> g_profiling{false};
+std::mutex g_prof_mu;
+struct ProfRec {
+    cudaEvent_t a, b;
+    int cls;
+};
+std::vector<ProfRec> g_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return e;
+}
+
+template <typename F>
+int counted_launch(int cls, cudaStream_t s, F&& fn) {
+    ProfRec rec{nullptr, nullptr, cls};
+    const bool prof = g_profiling.load();
+    if (prof) {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        rec.a = take_event();
+        rec.b = take_event();
+        if (rec.a) cudaEventRecord(rec.a, s);
+    }
+    const int r = fn();
+    g_launches.fetch_add(1);
+    if (prof && rec.a && rec.b) {
+        cudaEventRecord(rec.b, s);
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        g_recs.push_back(rec);
+    }
+    return r;
+}
+
+#define LAUNCH(cls, call) CK(counted_launch((cls), s, [&]() { return static_cast<int>(call); }))
 
 // ------------------------------------------------------------ tensor maps
 
@@ -232,7 +287,7 @@ int run_phase(DeviceState& st, int G, int bn, const ProblemSpec& p0, const Probl
     }
     ph.total_tiles = total;
     ph.err = st.err;
-    CK(launch_gemm_phase(ph, bn, st.num_sms, s));
+    LAUNCH(kClsGemm, launch_gemm_phase(ph, bn, st.num_sms, s));
     return GNS_OK;
 }
 
@@ -356,7 +411,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     {
         const Mat& direct = g.transposed ? XTa : Xa;
         const Mat& trans = g.transposed ? Xa : XTa;
-        CK(launch_scale_cast(in, Gc, g.R, g.C, reinterpret_cast<const float*>(ws + L.partial), nblk, g.k_exp,
+        LAUNCH(kClsCast, launch_scale_cast(in, Gc, g.R, g.C, reinterpret_cast<const float*>(ws + L.partial), nblk, g.k_exp,
                              direct.p, direct.ld, direct.stride, trans.p, trans.ld, trans.stride, st.err, s));
     }
     const float inv_s = 1.0f / g.s;
@@ -564,7 +619,7 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart
         const int gc = std::min(Gc, G - g0);
         float* base = ptr + static_cast<long long>(g0) * numel;
         MatrixSet in{base, numel, nullptr};
-        CK(launch_sumsq(in, numel, gc, reinterpret_cast<float*>(st->ws + L.partial), st->err, s));
+        LAUNCH(kClsNorm, launch_sumsq(in, numel, gc, reinterpret_cast<float*>(st->ws + L.partial), st->err, s));
         OutSpec os;
         if (direct_out) {
             os.out.p = base;
@@ -583,7 +638,7 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart
         }
         RET(run_core(*st, g, L, gc, in, nblk, steps, restart_at, cf, os, s));
         if (!direct_out)
-            CK(launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
+            LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
     }
     return GNS_OK;
 }
@@ -689,7 +744,7 @@ int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tenso
             MatrixSet Gs{nullptr, 0, pm + gc};
             MatrixSet Ws{nullptr, 0, pm + 2 * gc};
             float* partial = reinterpret_cast<float*>(st->ws + L.partial);
-            CK(launch_momentum(Ms, Gs, numel, gc, mu, partial, s));
+            LAUNCH(kClsMuon, launch_momentum(Ms, Gs, numel, gc, mu, partial, s));
             OutSpec os;
             os.out.p = st->ws + L.o16;
             os.out.rows = R;
@@ -699,7 +754,7 @@ int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tenso
             os.out.f32 = false;
             RET(run_core(*st, g, L, gc, Ms, norm_blocks(numel), 5, 2, cf, os, s));
             MatrixSet Os{os.out.p, os.out.stride, nullptr};
-            CK(launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s));
+            LAUNCH(kClsMuon, launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s));
         }
     }
     return GNS_OK;
@@ -712,7 +767,8 @@ int gns_muon_momentum(float* M, const uint16_t* G_bf16, int64_t numel, float mu,
     RET(get_state(&st));
     MatrixSet Ms{M, numel, nullptr};
     MatrixSet Gs{G_bf16, numel, nullptr};
-    CK(launch_momentum(Ms, Gs, numel, 1, mu, nullptr, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    LAUNCH(kClsMuon, launch_momentum(Ms, Gs, numel, 1, mu, nullptr, s));
     return GNS_OK;
 }
 
@@ -726,8 +782,8 @@ int gns_muon_update(uint16_t* W_bf16, const uint16_t* O_fp16, int rows, int cols
     const long long numel = static_cast<long long>(rows) * cols;
     MatrixSet Ws{W_bf16, numel, nullptr};
     MatrixSet Os{O_fp16, numel, nullptr};
-    CK(launch_muon_update(Ws, Os, cols, nullptr, base_index, 1, rows, cols, lr, wd, scale, seed, step,
-                          static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    LAUNCH(kClsMuon, launch_muon_update(Ws, Os, cols, nullptr, base_index, 1, rows, cols, lr, wd, scale, seed, step, s));
     return GNS_OK;
 }
 
@@ -779,6 +835,44 @@ const char* gns_status_string(int status) {
 }
 
 const char* gns_last_error(void) { return g_last_error.c_str(); }
+
+int64_t gns_launch_count(void) { return g_launches.load(); }
+
+void gns_profile_enable(int on) { g_profiling.store(on != 0); }
+
+int gns_profile_read(int64_t* counts, double* ms, int max_classes) {
+    std::vector<ProfRec> recs;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        recs.swap(g_recs);
+    }
+    std::vector<int64_t> c(kNumCls, 0);
+    std::vector<double> t(kNumCls, 0.0);
+    int rc = GNS_OK;
+    for (auto& r : recs) {
+        float e = 0.0f;
+        cudaError_t err = cudaEventSynchronize(r.b);
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&e, r.a, r.b);
+        if (err != cudaSuccess) {
+            rc = cuda_fail(err, "cudaEventElapsedTime");
+        } else {
+            c[r.cls] += 1;
+            t[r.cls] += e;
+        }
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        for (auto& r : recs) {
+            g_event_pool.push_back(r.a);
+            g_event_pool.push_back(r.b);
+        }
+    }
+    for (int k = 0; k < kNumCls && k < max_classes; ++k) {
+        if (counts) counts[k] = c[k];
+        if (ms) ms[k] = t[k];
+    }
+    return rc == GNS_OK ? kNumCls : rc;
+}
 
 int64_t gns_workspace_bytes(void) {
     int dev = 0;
