@@ -82,6 +82,31 @@ int gns_orthogonalize_batched(float* ptr, int G, int R, int C, int steps, int re
 int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int steps,
                                    int restart_at, const float* coeffs, void* stream);
 
+/*
+ * gns_orthogonalize_batched_noalloc: gns_orthogonalize_batched without any
+ * device allocation, for callers that cannot let a library call cudaMalloc
+ * (their device memory is already held by their own allocator or pool, or
+ * they cannot accept the device-wide synchronization that growing the cached
+ * workspace costs). The paper has no counterpart; this is a library entry
+ * point only.
+ *
+ * Arguments, layout and results are those of gns_orthogonalize_batched (the
+ * results are bit-identical). The workspace is one fixed 64 MiB array in
+ * device memory that every GPU which loads the library holds until the
+ * process exits; the bucket is processed in as many sequential chunks as
+ * that space requires. A matrix whose workspace alone exceeds it (for
+ * example 4096 x 14336) is rejected with GNS_ERR_INVALID and a message in
+ * gns_last_error(). The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call shares the array, so calls that overlap on the GPU (on
+ * different streams) race and must not be issued. Device-side conditions (a
+ * non-finite input norm, a bounded wait that ran out) go to a status word
+ * inside the array, cleared at the start of each call; gns_get_status() does
+ * not read it.
+ */
+int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C, int steps, int restart_at,
+                                      const float* coeffs, void* stream);
+
 /* One 2D tensor of a Muon step. data is a device pointer; rows x cols,
  * row-major, contiguous. base_index is the global index of element (0, 0)
  * for the stochastic-rounding counter (the Muon kernel card: a parameter

@@ -13,7 +13,8 @@ import torch
 
 from ._lib import GnsError, GnsTensor, check, load
 
-__all__ = ["gns_orthogonalize_batched", "gns_orthogonalize_batched_host", "muon_step",
+__all__ = ["gns_orthogonalize_batched", "gns_orthogonalize_batched_host",
+           "gns_orthogonalize_batched_noalloc", "muon_step",
            "gns_muon_momentum", "gns_muon_update", "gns_symm_gemm", "gns_get_status",
            "gns_status_string", "gns_last_error", "gns_workspace_bytes", "gns_release",
            "gns_launch_count", "gns_profile_enable", "gns_profile_read", "KERNEL_CLASSES",
@@ -72,6 +73,20 @@ def gns_orthogonalize_batched_host(x, steps=5, restart_at=2, coeffs=None, stream
     dev = torch.device("cuda", torch.cuda.current_device())
     check(lib.gns_orthogonalize_batched_host(ctypes.c_void_p(x.data_ptr()), G, R, C, steps, restart_at,
                                              cptr, _stream(stream, dev)), "gns_orthogonalize_batched_host")
+    del keep
+    return x
+
+
+def gns_orthogonalize_batched_noalloc(x, steps=5, restart_at=2, coeffs=None, stream=None):
+    """gns_orthogonalize_batched through the allocation-free entry point: the
+    library's workspace is its fixed device array, never cudaMalloc."""
+    _require(x, torch.float32, name="x")
+    G, R, C = (1, *x.shape) if x.dim() == 2 else tuple(x.shape)
+    keep, cptr = _coeff_array(coeffs, steps)
+    lib = load()
+    check(lib.gns_orthogonalize_batched_noalloc(ctypes.c_void_p(x.data_ptr()), G, R, C, steps, restart_at,
+                                                cptr, _stream(stream, x.device)),
+          "gns_orthogonalize_batched_noalloc")
     del keep
     return x
 

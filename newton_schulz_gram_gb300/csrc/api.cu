@@ -904,3 +904,115 @@ void gns_release(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of gns_orthogonalize_batched.
+//
+// Some callers cannot let the library call cudaMalloc: their device memory is
+// already held by their own allocator or pool, or they cannot accept the
+// device-wide synchronization that growing the cached workspace costs
+// (cudaDeviceSynchronize, cudaFree, cudaMalloc). For them the workspace of
+// this entry point is one fixed array in device memory, declared below, that
+// every GPU which loads the library holds until the process exits.
+
+namespace gns {
+namespace {
+
+constexpr size_t kNoAllocBytes = size_t(64) << 20;  // size of the fixed array
+constexpr size_t kNoAllocStatusBytes = 256;         // status word, then the workspace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+    bool ready = false;
+    char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+
+std::mutex g_noalloc_mu;
+std::map<int, NoAllocDevice> g_noalloc;
+
+}  // namespace
+}  // namespace gns
+
+extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C, int steps, int restart_at,
+                                                 const float* coeffs, void* stream) {
+    RET(validate_common(G, R, C, steps));
+    if (G == 0) return GNS_OK;
+    if (!ptr) return fail(GNS_ERR_INVALID, "ptr is null");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    NoAllocDevice nd;
+    {
+        // First call on a device: look up the array's device address (the
+        // name is only a host-side stand-in) and the SM count. No allocation.
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        NoAllocDevice& e = g_noalloc[dev];
+        if (!e.ready) {
+            CK(cudaDeviceGetAttribute(&e.num_sms, cudaDevAttrMultiProcessorCount, dev));
+            CK(cudaDeviceGetAttribute(&e.cc_major, cudaDevAttrComputeCapabilityMajor, dev));
+            CK(cudaDeviceGetAttribute(&e.cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
+            void* addr = nullptr;
+            CK(cudaGetSymbolAddress(&addr, g_noalloc_scratch));
+            e.scratch = static_cast<char*>(addr);
+            e.ready = true;
+        }
+        nd = e;
+    }
+    if (!(nd.cc_major == 10 && nd.cc_minor == 3))
+        return fail(GNS_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300) only");
+    Coeffs cf;
+    RET(load_coeffs(coeffs, steps, cf));
+    const BucketGeom g = make_geom(R, C);
+    const bool direct_out = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && ((static_cast<long long>(C) * 4) % 16 == 0);
+    // Largest chunk of matrices whose workspace fits in the fixed array.
+    const size_t avail = kNoAllocBytes - kNoAllocStatusBytes;
+    const size_t per = make_layout(g, 1, !direct_out, false, 0).total;
+    if (per > avail)
+        return fail(GNS_ERR_INVALID, "a " + std::to_string(R) + " x " + std::to_string(C) + " matrix needs " +
+                                         std::to_string(per) + " bytes of workspace; the allocation-free entry point has " +
+                                         std::to_string(avail) + " bytes");
+    int Gc = static_cast<int>(std::min<size_t>(std::min<size_t>(G, 65535), avail / per));
+    while (Gc > 1 && make_layout(g, Gc, !direct_out, false, 0).total > avail) --Gc;
+    const Layout L = make_layout(g, Gc, !direct_out, false, 0);
+
+    DeviceState st;
+    st.device = dev;
+    st.num_sms = nd.num_sms;
+    st.cc_major = nd.cc_major;
+    st.cc_minor = nd.cc_minor;
+    st.err = reinterpret_cast<int*>(nd.scratch);
+    st.ws = nd.scratch + kNoAllocStatusBytes;
+    st.ws_bytes = avail;
+    // The array keeps the previous call's contents; only the status word must
+    // start at zero (every workspace byte a kernel reads is written first).
+    CK(cudaMemsetAsync(st.err, 0, sizeof(int), s));
+
+    const long long numel = static_cast<long long>(R) * C;
+    const int nblk = norm_blocks(numel);
+    for (int g0 = 0; g0 < G; g0 += Gc) {
+        const int gc = std::min(Gc, G - g0);
+        float* base = ptr + static_cast<long long>(g0) * numel;
+        MatrixSet in{base, numel, nullptr};
+        LAUNCH(kClsNorm, launch_sumsq(in, numel, gc, reinterpret_cast<float*>(st.ws + L.partial), st.err, s));
+        OutSpec os;
+        os.out.rows = R;
+        os.out.cols = C;
+        os.out.f32 = true;
+        if (direct_out) {
+            os.out.p = base;
+            os.out.ld = C;
+            os.out.stride = numel;
+        } else {
+            os.out.p = st.ws + L.out32;
+            os.out.ld = L.ld_out32;
+            os.out.stride = static_cast<long long>(R) * L.ld_out32;
+        }
+        RET(run_core(st, g, L, gc, in, nblk, steps, restart_at, cf, os, s));
+        if (!direct_out)
+            LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
+    }
+    return GNS_OK;
+}
