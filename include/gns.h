@@ -169,7 +169,8 @@ int gns_muon_update(uint16_t* W_bf16, const uint16_t* O_fp16, int rows, int cols
  *      product X X^T when B == A; A B when B is symmetric and k == n).
  *   C  device fp16 [G][n][n] (exactly symmetric) or NULL (beta ignored).
  *   D  device fp16 [G][n][n], written.
- * n and k must be multiples of 8 (16-byte rows). Asynchronous.
+ * n and k must be multiples of 8 (16-byte rows) and every pointer 16-byte
+ * aligned. Asynchronous.
  */
 int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, int n, int k,
                   float alpha, float beta, void* stream);

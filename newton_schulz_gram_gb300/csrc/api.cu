@@ -227,69 +227,165 @@ struct ProblemSpec {
     const Mat* D2t = nullptr;
     float alpha = 1.f, beta = 0.f, delta = 0.f, gamma = 0.f;
     bool sym = false;
+    bool reverse = false;  // visit matrices last to first (starts on L2-resident data)
 };
 
-int set_problem(GemmProblem& pr, const ProblemSpec& sp, int G, int bn, int tile_begin) {
-    std::memset(&pr, 0, sizeof(pr));
-    if (sp.A.cols != sp.B.cols) return fail(GNS_ERR_INVALID, "operand K mismatch");
-    if ((sp.sym || sp.D2) && bn != 128) return fail(GNS_ERR_INVALID, "symmetric/second-output phases need 128-wide tiles");
-    if (sp.sym && sp.A.rows != sp.B.rows) return fail(GNS_ERR_INVALID, "symmetric product must be square");
-    if (sp.D2 && sp.Dt && !sp.D2t) return fail(GNS_ERR_INVALID, "second output needs its transposed map");
-    if (sp.D.f32 && (sp.Dt || sp.D2)) return fail(GNS_ERR_INVALID, "fp32 output supports no transposed/second output");
-    if (G > 65535) return fail(GNS_ERR_INVALID, "too many matrices in one launch");
-    RET(make_map(&pr.tmA, sp.A, G, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-    RET(make_map(&pr.tmB, sp.B, G, 64, bn, CU_TENSOR_MAP_SWIZZLE_128B));
-    RET(make_map(&pr.tmD, sp.D, G, 32, 32, sp.D.f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B));
-    int flags = 0;
-    if (sp.sym) flags |= kFlagSym;
-    if (sp.D.f32) flags |= kFlagOutF32;
-    if (sp.C) {
-        flags |= kFlagC;
-        pr.C = static_cast<const __half*>(sp.C->p);
-        pr.ldc = sp.C->ld;
-        pr.strideC = sp.C->stride;
+// Tile shape for a program: 256 x 256 tiles on CTA pairs when the matrices
+// fill them, else 128 x 128 tiles on single CTAs. GNS_TILE=128x1|256x1|256x2
+// forces one shape (tuning).
+struct TileShape {
+    int bn, cg;
+};
+
+TileShape choose_tile(int n) {
+    const char* force = std::getenv("GNS_TILE");
+    if (force) {
+        const std::string f(force);
+        if (f == "128x1") return {128, 1};
+        if (f == "256x1") return {256, 1};
+        if (f == "256x2") return {256, 2};
     }
-    if (sp.Dt) {
-        flags |= kFlagDt;
-        RET(make_map(&pr.tmDt, *sp.Dt, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
-    }
-    if (sp.D2) {
-        flags |= kFlagD2;
-        RET(make_map(&pr.tmD2, *sp.D2, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
-        if (sp.D2t) RET(make_map(&pr.tmD2t, *sp.D2t, G, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
-    }
-    pr.alpha = sp.alpha;
-    pr.beta = sp.beta;
-    pr.delta = sp.delta;
-    pr.gamma = sp.gamma;
-    pr.M = sp.A.rows;
-    pr.N = sp.B.rows;
-    pr.K = sp.A.cols;
-    pr.G = G;
-    pr.tiles_m = (pr.M + 127) / 128;
-    pr.tiles_n = (pr.N + bn - 1) / bn;
-    pr.tiles_per_matrix = sp.sym ? pr.tiles_m * (pr.tiles_m + 1) / 2 : pr.tiles_m * pr.tiles_n;
-    pr.tile_begin = tile_begin;
-    pr.flags = flags;
-    return GNS_OK;
+    return n >= 192 ? TileShape{256, 2} : TileShape{128, 1};
 }
 
-int run_phase(DeviceState& st, int G, int bn, const ProblemSpec& p0, const ProblemSpec* p1, cudaStream_t s) {
-    GemmPhase ph;
-    std::memset(&ph, 0, sizeof(ph));
-    RET(set_problem(ph.prob[0], p0, G, bn, 0));
-    ph.nprob = 1;
-    int total = ph.prob[0].tiles_per_matrix * G;
-    if (p1) {
-        RET(set_problem(ph.prob[1], *p1, G, bn, total));
-        ph.nprob = 2;
-        total += ph.prob[1].tiles_per_matrix * G;
+// Collects the phases of one launch. Tensor maps are shared between the
+// problems that read or write the same buffer with the same box.
+class ProgramBuilder {
+  public:
+    ProgramBuilder(DeviceState& st, int G, TileShape ts, int* counters, cudaStream_t s)
+        : st_(st), G_(G), ts_(ts), counters_(counters), s_(s) {
+        reset();
     }
-    ph.total_tiles = total;
-    ph.err = st.err;
-    LAUNCH(kClsGemm, launch_gemm_phase(ph, bn, st.num_sms, s));
-    return GNS_OK;
-}
+
+    // Adds a phase of one or two independent problems; launches first when
+    // the program is full (the next launch then depends on it by stream order).
+    int phase(const ProblemSpec& p0, const ProblemSpec* p1, bool reverse) {
+        const int need_probs = p1 ? 2 : 1;
+        if (prog_.nphase + 1 > kMaxPhases || prog_.nprob + need_probs > kMaxProblems || prog_.nmaps + 12 > kMaxMaps)
+            RET(flush());
+        GemmPhaseDesc& ph = prog_.phase[prog_.nphase];
+        ph.prob_begin = prog_.nprob;
+        ph.nprob = 0;
+        ph.tiles_per_matrix = 0;
+        ph.tile_begin = prog_.total_tiles;
+        ph.wait_tiles = tiles_per_matrix_done_;
+        // Within one launch the phases pipeline per matrix, so every phase
+        // visits the matrices in the same order; the alternating order only
+        // helps between separate launches.
+        ph.reverse = (reverse && prog_.nphase == 0) ? 1 : 0;
+        for (const ProblemSpec* sp : {&p0, p1}) {
+            if (!sp) continue;
+            GemmProblem& pr = prog_.prob[prog_.nprob];
+            RET(set_problem(pr, *sp));
+            ph.tiles_per_matrix += pr.tiles_per_matrix;
+            ph.nprob += 1;
+            prog_.nprob += 1;
+        }
+        tiles_per_matrix_done_ += ph.tiles_per_matrix;
+        prog_.total_tiles += ph.tiles_per_matrix * G_;
+        prog_.nphase += 1;
+        return GNS_OK;
+    }
+
+    int flush() {
+        if (prog_.nphase == 0) return GNS_OK;
+        if (prog_.nphase > 1) {
+            prog_.counters = counters_;
+            CK(cudaMemsetAsync(counters_, 0, sizeof(int) * static_cast<size_t>(G_), s_));
+        } else {
+            prog_.counters = nullptr;
+        }
+        prog_.err = st_.err;
+        prog_.G = G_;
+        cudaStream_t s = s_;
+        LAUNCH(kClsGemm, launch_gemm_program(prog_, ts_.bn, ts_.cg, st_.num_sms, s));
+        reset();
+        return GNS_OK;
+    }
+
+  private:
+    void reset() {
+        std::memset(&prog_, 0, sizeof(prog_));
+        keys_.clear();
+        tiles_per_matrix_done_ = 0;
+    }
+
+    int map_index(const Mat& x, uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle sw) {
+        const std::string key = std::to_string(reinterpret_cast<uintptr_t>(x.p)) + ":" + std::to_string(x.rows) + ":" +
+                                std::to_string(x.cols) + ":" + std::to_string(x.ld) + ":" + std::to_string(x.stride) +
+                                ":" + std::to_string(x.f32) + ":" + std::to_string(box_c) + ":" +
+                                std::to_string(box_r) + ":" + std::to_string(static_cast<int>(sw));
+        for (size_t i = 0; i < keys_.size(); ++i)
+            if (keys_[i] == key) return static_cast<int>(i);
+        if (prog_.nmaps >= kMaxMaps) return -1;
+        if (make_map(&prog_.maps[prog_.nmaps], x, G_, box_c, box_r, sw) != GNS_OK) return -2;
+        keys_.push_back(key);
+        return prog_.nmaps++;
+    }
+
+    // A tiles are 128 rows per CTA; B tiles bn / cg rows per CTA.
+    int operand(const Mat& x, uint32_t box_rows, int& idx) {
+        idx = map_index(x, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+        return idx >= 0 ? GNS_OK : (idx == -1 ? fail(GNS_ERR_INVALID, "tensor map table full") : GNS_ERR_INVALID);
+    }
+
+    int output(const Mat& x, int& idx) {
+        idx = map_index(x, 32, 32, x.f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        return idx >= 0 ? GNS_OK : (idx == -1 ? fail(GNS_ERR_INVALID, "tensor map table full") : GNS_ERR_INVALID);
+    }
+
+    int set_problem(GemmProblem& pr, const ProblemSpec& sp) {
+        std::memset(&pr, 0, sizeof(pr));
+        const int bn = ts_.bn, cg = ts_.cg;
+        if (sp.A.cols != sp.B.cols) return fail(GNS_ERR_INVALID, "operand K mismatch");
+        if (sp.sym && sp.A.rows != sp.B.rows) return fail(GNS_ERR_INVALID, "symmetric product must be square");
+        if (sp.D2 && sp.Dt && !sp.D2t) return fail(GNS_ERR_INVALID, "second output needs its transposed map");
+        if (sp.D.f32 && (sp.Dt || sp.D2)) return fail(GNS_ERR_INVALID, "fp32 output supports no transposed/second output");
+        if (G_ > 65535) return fail(GNS_ERR_INVALID, "too many matrices in one launch");
+        pr.mA = pr.mB = pr.mD = pr.mDt = pr.mD2 = pr.mD2t = -1;
+        RET(operand(sp.A, 128, pr.mA));
+        RET(operand(sp.B, static_cast<uint32_t>(bn / cg), pr.mB));
+        RET(output(sp.D, pr.mD));
+        int flags = 0;
+        if (sp.sym) flags |= kFlagSym;
+        if (sp.D.f32) flags |= kFlagOutF32;
+        if (sp.C) {
+            flags |= kFlagC;
+            pr.C = static_cast<const __half*>(sp.C->p);
+            pr.ldc = sp.C->ld;
+            pr.strideC = sp.C->stride;
+        }
+        if (sp.Dt) {
+            flags |= kFlagDt;
+            RET(output(*sp.Dt, pr.mDt));
+        }
+        if (sp.D2) {
+            flags |= kFlagD2;
+            RET(output(*sp.D2, pr.mD2));
+            if (sp.D2t) RET(output(*sp.D2t, pr.mD2t));
+        }
+        pr.alpha = sp.alpha;
+        pr.beta = sp.beta;
+        pr.delta = sp.delta;
+        pr.gamma = sp.gamma;
+        pr.M = sp.A.rows;
+        pr.N = sp.B.rows;
+        pr.K = sp.A.cols;
+        pr.tiles_n = (pr.N + bn - 1) / bn;
+        pr.tiles_per_matrix = gemm_tiles_per_matrix(pr.M, pr.N, bn, cg, sp.sym);
+        pr.flags = flags;
+        return GNS_OK;
+    }
+
+    DeviceState& st_;
+    int G_;
+    TileShape ts_;
+    int* counters_;
+    cudaStream_t s_;
+    GemmProgram prog_;
+    std::vector<std::string> keys_;
+    int tiles_per_matrix_done_ = 0;
+};
 
 // --------------------------------------------------------------- planner
 
@@ -354,7 +450,7 @@ BucketGeom make_geom(int R, int C) {
 
 // Workspace layout for a chunk of Gc matrices.
 struct Layout {
-    size_t xa, xta, xb, xtb, r, z, rz, qa, qb, partial, out32, o16, meta, total;
+    size_t xa, xta, xb, xtb, r, z, rz, qa, qb, partial, counters, out32, o16, meta, total;
     long long ld_out32;
 };
 
@@ -379,6 +475,7 @@ Layout make_layout(const BucketGeom& g, int Gc, bool need_out32, bool need_o16, 
     L.qa = g.square ? 0 : take(nn);
     L.qb = g.square ? 0 : take(nn);
     L.partial = take(static_cast<size_t>(Gc) * 64 * 4);
+    L.counters = take(static_cast<size_t>(Gc) * 4);
     L.ld_out32 = round_up_ll(g.C, 4);
     L.out32 = need_out32 ? take(static_cast<size_t>(g.R) * L.ld_out32 * 4 * Gc) : 0;
     L.o16 = need_o16 ? take(static_cast<size_t>(g.R) * round_up_ll(g.C, 8) * 2 * Gc) : 0;
@@ -402,6 +499,7 @@ Mat mat16(char* ws, size_t off, int rows, int cols, long long ld) {
 // partials are already in L.partial (nblk per matrix).
 int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in, int nblk, int steps,
              int restart_at, const Coeffs& cf, const OutSpec& os, cudaStream_t s) {
+    ProgramBuilder prog(st, Gc, choose_tile(g.n), reinterpret_cast<int*>(st.ws + L.counters), s);
     char* ws = st.ws;
     const int n = g.n, m = g.m;
     Mat Xa = mat16(ws, L.xa, n, m, g.ldm);
@@ -416,6 +514,12 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     }
     const float inv_s = 1.0f / g.s;
     const float out_scale = std::ldexp(1.0f, -g.k_exp);
+    // Consecutive phases visit the matrices in opposite orders, so each phase
+    // starts on the matrices the previous one wrote last (still in L2).
+    int phase_no = 0;
+    auto phase = [&](const ProblemSpec& p0, const ProblemSpec* p1) {
+        return prog.phase(p0, p1, (phase_no++ & 1) != 0);
+    };
 
     if (g.square) {
         // Dion3 Algorithm 1 with symmetric A = X X^T and B = b A + c A^2
@@ -431,7 +535,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             pa.D = A;
             pa.Dt = &A;
             pa.sym = true;
-            RET(run_phase(st, Gc, 128, pa, nullptr, s));
+            RET(phase(pa, nullptr));
             ProblemSpec pb;
             pb.A = A;
             pb.B = A;
@@ -441,7 +545,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             pb.alpha = cf.c[t] * inv_s;
             pb.beta = cf.b[t];
             pb.sym = true;
-            RET(run_phase(st, Gc, 128, pb, nullptr, s));
+            RET(phase(pb, nullptr));
             ProblemSpec px;
             px.A = B;
             px.B = XT;
@@ -451,17 +555,17 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
                 px.Dt = &XTn;
                 px.alpha = inv_s;
                 px.beta = cf.a[t];
-                RET(run_phase(st, Gc, 256, px, nullptr, s));
+                RET(phase(px, nullptr));
                 std::swap(X, Xn);
                 std::swap(XT, XTn);
             } else {
                 px.D = os.out;
                 px.alpha = inv_s * out_scale;
                 px.beta = cf.a[t] * out_scale;
-                RET(run_phase(st, Gc, 256, px, nullptr, s));
+                RET(phase(px, nullptr));
             }
         }
-        return GNS_OK;
+        return prog.flush();
     }
 
     // Dion3 Algorithm 3 with the App. B.2.3 a-term distribution.
@@ -479,7 +583,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
         p.D = R;
         p.Dt = &R;
         p.sym = true;
-        return run_phase(st, Gc, 128, p, nullptr, s);
+        return phase(p, nullptr);
     };
     RET(gram());
     bool q_identity = true;
@@ -492,7 +596,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             p.B = XT;
             p.D = X;  // X is not read by this phase
             p.Dt = &XTn;
-            RET(run_phase(st, Gc, 256, p, nullptr, s));
+            RET(phase(p, nullptr));
             std::swap(XT, XTn);
             RET(gram());
             q_identity = true;
@@ -515,7 +619,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
                 p.delta = inv_s;
                 p.gamma = a;
             }
-            RET(run_phase(st, Gc, 128, p, nullptr, s));
+            RET(phase(p, nullptr));
         }
         ProblemSpec pq, prz;
         if (!q_identity) {
@@ -539,11 +643,11 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             prz.sym = true;
         }
         if (!q_identity && need_r) {
-            RET(run_phase(st, Gc, 128, pq, &prz, s));
+            RET(phase(pq, &prz));
         } else if (!q_identity) {
-            RET(run_phase(st, Gc, 128, pq, nullptr, s));
+            RET(phase(pq, nullptr));
         } else if (need_r) {
-            RET(run_phase(st, Gc, 128, prz, nullptr, s));
+            RET(phase(prz, nullptr));
         }
         if (!q_identity) std::swap(Qc, Qn);
         q_identity = false;
@@ -557,7 +661,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             p.alpha = inv_s;
             p.beta = a;
             p.sym = true;
-            RET(run_phase(st, Gc, 128, p, nullptr, s));
+            RET(phase(p, nullptr));
         }
     }
     // O = Q X, written in the caller's orientation.
@@ -571,8 +675,8 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     }
     p.D = os.out;
     p.alpha = out_scale;
-    RET(run_phase(st, Gc, 256, p, nullptr, s));
-    return GNS_OK;
+    RET(phase(p, nullptr));
+    return prog.flush();
 }
 
 size_t chunk_cap_bytes() {
@@ -793,6 +897,8 @@ int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, i
     if (G == 0) return GNS_OK;
     if (!A || !B || !D) return fail(GNS_ERR_INVALID, "null pointer");
     if (n % 8 || k % 8) return fail(GNS_ERR_INVALID, "n and k must be multiples of 8");
+    for (const void* q : {A, B, C, static_cast<const void*>(D)})
+        if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return fail(GNS_ERR_INVALID, "pointers must be 16-byte aligned");
     DeviceState* st = nullptr;
     RET(get_state(&st));
     Mat a{const_cast<void*>(A), n, k, k, static_cast<long long>(n) * k, false};
@@ -808,7 +914,10 @@ int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, i
     p.alpha = alpha;
     p.beta = C ? beta : 0.0f;
     p.sym = true;
-    return run_phase(*st, G, 128, p, nullptr, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ProgramBuilder prog(*st, G, choose_tile(n), nullptr, s);
+    RET(prog.phase(p, nullptr, false));
+    return prog.flush();
 }
 
 int gns_get_status(void* stream) {

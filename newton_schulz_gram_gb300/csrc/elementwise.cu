@@ -24,6 +24,24 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Launch with the programmatic-dependent-launch attribute; every kernel here
+// starts with grid_dependency_wait(), so it reads nothing the previous grid
+// writes before that grid has completed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ const float* mat_f32(const MatrixSet& s, int g) {
     return s.ptrs ? static_cast<const float*>(s.ptrs[g])
                   : static_cast<const float*>(s.base) + static_cast<long long>(g) * s.stride;
@@ -79,6 +97,8 @@ __device__ __forceinline__ float chunk_sumsq(const float* x, long long beg, long
 
 __global__ void __launch_bounds__(kThreads) sumsq_kernel(MatrixSet in, long long numel, int nblk,
                                                          float* partial) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const float* x = mat_f32(in, blockIdx.y);
     const long long chunk = chunk_len(numel, nblk);
     const long long beg = static_cast<long long>(blockIdx.x) * chunk;
@@ -97,6 +117,8 @@ __global__ void __launch_bounds__(kThreads) scale_cast_kernel(MatrixSet in, int 
                                                               long long ld_t, long long stride_t, int* err) {
     __shared__ float tile[TILE][TILE + 1];
     __shared__ float s_scale;
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int g = blockIdx.z;
     if (threadIdx.x == 0) {
         float t = 0.0f;
@@ -175,6 +197,8 @@ __global__ void __launch_bounds__(kThreads) scale_cast_kernel(MatrixSet in, int 
 
 __global__ void __launch_bounds__(kThreads) copy_rows_kernel(const float* in, long long ld_in, long long stride_in,
                                                              float* out, int R, int C) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int g = blockIdx.y;
     const long long numel = static_cast<long long>(R) * C;
     for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < numel;
@@ -186,6 +210,8 @@ __global__ void __launch_bounds__(kThreads) copy_rows_kernel(const float* in, lo
 
 __global__ void __launch_bounds__(kThreads) momentum_kernel(MatrixSet Ms, MatrixSet Gs, long long numel, int nblk,
                                                             float mu, float* partial) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int g = blockIdx.y;
     float* M = mat_ptr<float>(Ms, g);
     const __nv_bfloat16* Gr = mat_ptr<const __nv_bfloat16>(Gs, g);
@@ -260,6 +286,8 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
                                                                const long long* base_dev, long long base_scalar,
                                                                int R, int C, float lr, float wd, float scale,
                                                                uint32_t k0, uint32_t k1, uint32_t s0, uint32_t s1) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int g = blockIdx.y;
     uint16_t* W = mat_ptr<uint16_t>(Ws, g);
     const __half* O = mat_ptr<const __half>(Os, g);
@@ -333,8 +361,7 @@ int launch_sumsq(const MatrixSet& in, long long numel, int G, float* partial, in
     (void)err;
     if (G <= 0 || numel <= 0) return cudaSuccess;
     const int nblk = norm_blocks(numel);
-    sumsq_kernel<<<dim3(nblk, G), kThreads, 0, s>>>(in, numel, nblk, partial);
-    return cudaGetLastError();
+    return launch_pdl(sumsq_kernel, dim3(nblk, G), dim3(kThreads), s, in, numel, nblk, partial);
 }
 
 int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* partial, int nblk, int k_exp,
@@ -342,26 +369,24 @@ int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* par
                       long long stride_trans, int* err, cudaStream_t s) {
     if (G <= 0) return cudaSuccess;
     dim3 grid((C + TILE - 1) / TILE, (R + TILE - 1) / TILE, G);
-    scale_cast_kernel<<<grid, kThreads, 0, s>>>(in, R, C, partial, nblk, k_exp, static_cast<__half*>(direct),
-                                                 ld_direct, stride_direct, static_cast<__half*>(trans), ld_trans,
-                                                 stride_trans, err);
-    return cudaGetLastError();
+    return launch_pdl(scale_cast_kernel, grid, dim3(kThreads), s, in, R, C, partial, nblk, k_exp,
+                      static_cast<__half*>(direct), ld_direct, stride_direct, static_cast<__half*>(trans), ld_trans,
+                      stride_trans, err);
 }
 
 int launch_copy_rows_f32(const float* in, long long ld_in, long long stride_in, float* out, int G, int R, int C,
                          cudaStream_t s) {
     if (G <= 0) return cudaSuccess;
     const long long numel = static_cast<long long>(R) * C;
-    copy_rows_kernel<<<dim3(grid_for(numel, kThreads * 8), G), kThreads, 0, s>>>(in, ld_in, stride_in, out, R, C);
-    return cudaGetLastError();
+    return launch_pdl(copy_rows_kernel, dim3(grid_for(numel, kThreads * 8), G), dim3(kThreads), s, in, ld_in,
+                      stride_in, out, R, C);
 }
 
 int launch_momentum(const MatrixSet& M, const MatrixSet& Gr, long long numel, int count, float mu, float* partial,
                     cudaStream_t s) {
     if (count <= 0 || numel <= 0) return cudaSuccess;
     const int nblk = partial ? norm_blocks(numel) : grid_for(numel, kThreads * 16);
-    momentum_kernel<<<dim3(nblk, count), kThreads, 0, s>>>(M, Gr, numel, nblk, mu, partial);
-    return cudaGetLastError();
+    return launch_pdl(momentum_kernel, dim3(nblk, count), dim3(kThreads), s, M, Gr, numel, nblk, mu, partial);
 }
 
 int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o, const long long* base_dev,
@@ -369,10 +394,10 @@ int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o, c
                        uint64_t seed, uint64_t step, cudaStream_t s) {
     if (count <= 0 || static_cast<long long>(R) * C <= 0) return cudaSuccess;
     const long long groups = static_cast<long long>(R) * C / 4 + 2;
-    muon_update_kernel<<<dim3(grid_for(groups, kThreads * 4), count), kThreads, 0, s>>>(
-        W, O, ld_o, base_dev, base_scalar, R, C, lr, wd, scale, static_cast<uint32_t>(seed),
-        static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32));
-    return cudaGetLastError();
+    return launch_pdl(muon_update_kernel, dim3(grid_for(groups, kThreads * 4), count), dim3(kThreads), s, W, O,
+                      ld_o, base_dev, base_scalar, R, C, lr, wd, scale, static_cast<uint32_t>(seed),
+                      static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(step),
+                      static_cast<uint32_t>(step >> 32));
 }
 
 }  // namespace gns

@@ -1,11 +1,18 @@
 // Shared (host and device) description of one grouped GEMM launch.
 //
-// A launch ("phase") runs up to two independent problems. Each problem is a
-// batch of G equal-shaped products D_g = alpha * A_g B_g^T (+ beta * C_g),
-// fp16 operands, fp32 accumulation, where A_g is M x K and B_g is N x K, both
-// row-major (K contiguous). For a symmetric product (Dion3 §5) only the
-// lower-triangle 128 x 128 tiles are computed and each is also written
-// transposed into the upper triangle.
+// A launch runs a "program": a sequence of phases over a bucket of G
+// matrices. Each phase holds one or more independent problems; a problem is
+// a batch of G equal-shaped products D_g = alpha * A_g B_g^T (+ beta * C_g),
+// fp16 operands, fp32 accumulation, A_g M x K and B_g N x K row-major (K
+// contiguous). For a symmetric product (Dion3 §5) only the tiles touching the
+// lower triangle are computed and each is also written transposed into the
+// upper triangle.
+//
+// Tiles are numbered phase by phase, matrix by matrix. When the program has
+// more than one phase, a tile of phase s on matrix g starts only once every
+// tile of the earlier phases on matrix g has been stored (per-matrix counters
+// in global memory, release/acquire), so different matrices pipeline through
+// the phases without a grid-wide barrier.
 #pragma once
 
 #include <cstdint>
@@ -15,41 +22,58 @@
 namespace gns {
 
 enum GemmFlags : int {
-    kFlagSym = 1,     // triangular tile list, mirrored epilogue (M == N, BN == 128)
+    kFlagSym = 1,     // lower-triangle tile list, mirrored epilogue (M == N)
     kFlagC = 2,       // add beta * C (fp16, row-major, same shape as D)
-    kFlagDt = 4,      // also write D transposed through tmDt
-    kFlagD2 = 8,      // also write D2 = delta * D + gamma * I (fp16) through tmD2 (+ tmD2t)
+    kFlagDt = 4,      // also write D transposed into Dt ([G][N][M])
+    kFlagD2 = 8,      // also write D2 = delta * D + gamma * I (fp16), and its mirror D2t
     kFlagOutF32 = 16  // D is fp32 (otherwise fp16)
 };
 
-struct alignas(128) GemmProblem {
-    CUtensorMap tmA;    // [G][M][K] fp16, box {64, 128}, 128-byte swizzle
-    CUtensorMap tmB;    // [G][N][K] fp16, box {64, BN}, 128-byte swizzle
-    CUtensorMap tmD;    // [G][M][N] fp16 (box {32,32}, 64B swizzle) or fp32 (box {32,32}, 128B swizzle)
-    CUtensorMap tmDt;   // [G][N][M] fp16, box {32, 32}, no swizzle
-    CUtensorMap tmD2;   // [G][M][N] fp16, as tmD
-    CUtensorMap tmD2t;  // [G][N][M] fp16, as tmDt
-    const __half* C;    // addend, row-major [G][M][ldc]
+constexpr int kMaxMaps = 24;
+constexpr int kMaxProblems = 48;
+constexpr int kMaxPhases = 40;
+
+struct GemmProblem {
+    const __half* C;  // addend, row-major [G][M][ldc]
     long long ldc;
     long long strideC;
     float alpha, beta, delta, gamma;
-    int M, N, K, G;
-    int tiles_m, tiles_n, tiles_per_matrix, tile_begin;
+    int M, N, K;
+    int tiles_n, tiles_per_matrix;
     int flags;
-    int pad_;
+    // Indices into GemmProgram::maps (-1 when unused). Operand maps: box
+    // {64, 128}, 128-byte swizzle. Output maps: box {32, 32}, 64-byte swizzle
+    // (fp16) or 128-byte swizzle (fp32).
+    int mA, mB, mD, mDt, mD2, mD2t;
 };
 
-struct alignas(128) GemmPhase {
-    GemmProblem prob[2];
+struct GemmPhaseDesc {
+    int prob_begin, nprob;  // problems prob[prob_begin .. prob_begin + nprob)
+    int tiles_per_matrix;   // over all its problems
+    int tile_begin;         // program-wide index of its first tile
+    int wait_tiles;         // tiles per matrix of all earlier phases
+    int reverse;            // visit matrices last to first
+};
+
+struct alignas(128) GemmProgram {
+    CUtensorMap maps[kMaxMaps];
+    GemmProblem prob[kMaxProblems];
+    GemmPhaseDesc phase[kMaxPhases];
+    int* counters;  // [G] completed-tile counters, zero at launch; null for one phase
     int* err;
-    int nprob;
-    int total_tiles;
+    int nmaps, nprob, nphase, G, total_tiles;
 };
 
-// Host-side launchers (gemm_tc.cu). `bn` selects the tile width: 128 for
-// symmetric phases (and those with a second output), 256 for the general
-// products. Return a cudaError_t value.
-int launch_gemm_phase(const GemmPhase& phase, int bn, int num_sms, cudaStream_t stream);
-int gemm_smem_bytes(int bn);
+// Host-side launcher (gemm_tc.cu). Tile shapes: cg = 1 and bn = 128 or 256
+// (one CTA, 128 x bn tiles), or cg = 2 and bn = 256 (a CTA pair, 256 x 256
+// tiles with paired MMAs). Launches carry the programmatic-dependent-launch
+// attribute; the kernel waits for the previous grid before reading its
+// operands. Returns a cudaError_t value.
+int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream);
+int gemm_smem_bytes(int bn, int cg);
+// Tiles one matrix of an M x N problem needs (lower-triangle tiles if sym).
+int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym);
+// Counter increments one tile contributes (one per epilogue warp).
+int gemm_signals_per_tile(int cg);
 
 }  // namespace gns

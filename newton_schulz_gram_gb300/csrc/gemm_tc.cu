@@ -1,6 +1,8 @@
 // Grouped, persistent tcgen05 GEMM for sm_103a.
 //
-// One CTA per SM walks the phase's tile list with a static stride. Warp roles:
+// One CTA (or CTA pair) per SM (pair of SMs) walks the program's tile list
+// with a static stride. Tiles of later phases wait, per matrix, for the
+// earlier phases' tiles of the same matrix (see gemm.cuh). Warp roles:
 //   warp 0      TMA producer: A and B k-blocks (64 fp16 = 128 B wide, 128-byte
 //               swizzle) into a STAGES-deep ring of shared-memory slots.
 //   warp 1      TMEM owner and MMA issuer: one thread issues
@@ -14,11 +16,16 @@
 //               "Epilogue: Writing to the Transposed Tile").
 //
 // Symmetric products (Dion3 §5 "Triangular Scheduler", App. C.1) visit only
-// tiles (i, j) with i >= j. Off-diagonal tiles write D(i, j) and D(j, i) =
-// D(i, j)^T. A diagonal tile writes its strictly-lower 32 x 32 sub-blocks
-// twice (direct and mirrored), its diagonal sub-blocks once after copying
-// their lower half onto their upper half, and skips its upper sub-blocks;
-// every element is written exactly once and D is exactly symmetric.
+// the 128 x BN tiles that touch the lower triangle (row block i holds the
+// column blocks j with j * BN <= 128 i + 127). Each 32 x 32 sub-block is then
+// classified by its global position: strictly lower sub-blocks are written
+// directly and mirrored, diagonal sub-blocks are written once after their
+// upper half is replaced by the transpose of their lower half, upper
+// sub-blocks are skipped. Every element is written exactly once and the
+// result is exactly symmetric.
+//
+// Transposed sub-blocks are built in shared memory with ldmatrix.trans /
+// stmatrix; all fp16 staging uses the 64-byte swizzle of its TMA maps.
 #include <cstdio>
 
 #include "gemm.cuh"
@@ -29,56 +36,85 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+static_assert(sizeof(GemmProgram) <= 32764, "kernel parameter block too large");
+constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 
-// Staging layout inside one per-warp epilogue buffer (bytes).
-constexpr int kOffD = 0;       // D sub-block: fp16 (2 KB, 64B swizzle) or fp32 (4 KB, 128B swizzle)
-constexpr int kOffDt = 2048;   // D^T sub-block, fp16, unswizzled 64-byte rows
-constexpr int kOffD2 = 4096;   // D2 sub-block
-constexpr int kOffD2t = 6144;  // D2^T sub-block
+// One per-warp epilogue staging buffer (bytes): four 32 x 32 fp16 blocks, or
+// one 32 x 32 fp32 block at kOffD.
+constexpr int SBUF = 8192;
+constexpr int kOffD = 0;
+constexpr int kOffDt = 2048;
+constexpr int kOffD2 = 4096;
+constexpr int kOffD2t = 6144;
 
-template <int BN>
+// Kernel variants: <BN, CG>. CG = 1: one CTA computes a 128 x BN tile.
+// CG = 2: a cluster of two CTAs computes a 256 x BN tile with paired MMAs
+// (tcgen05.mma.cta_group::2, M = 256); each CTA stages its 128 rows of A and
+// BN / 2 rows of B, so a stage costs half the shared memory per MMA.
+template <int BN, int CG>
 struct Cfg;
 template <>
-struct Cfg<128> {
+struct Cfg<128, 1> {
     static constexpr int STAGES = 5;
-    static constexpr int SBUF = 8192;  // D, D^T, D2, D2^T
 };
 template <>
-struct Cfg<256> {
-    static constexpr int STAGES = 4;
-    static constexpr int SBUF = 4096;  // D (fp32) or D + D^T (fp16)
+struct Cfg<256, 1> {
+    static constexpr int STAGES = 3;
+};
+template <>
+struct Cfg<256, 2> {
+    static constexpr int STAGES = 5;
 };
 
-template <int BN>
+template <int BN, int CG>
 constexpr int smem_bytes() {
-    return 1024 + Cfg<BN>::STAGES * (BM * BK * 2 + BN * BK * 2) + 4 * 2 * Cfg<BN>::SBUF +
-           (2 * Cfg<BN>::STAGES + 5) * 8 + 16;
+    return 1024 + Cfg<BN, CG>::STAGES * (BM * BK * 2 + (BN / CG) * BK * 2) + kEpiWarps * SBUF +
+           (2 * Cfg<BN, CG>::STAGES + 5) * 8 + 16;
 }
 
 struct TileInfo {
-    int p, g, m0, n0;
+    int p, g, m0, n0, s;  // problem, matrix, tile origin, phase
 };
 
-template <int BN>
-__device__ __forceinline__ TileInfo decode_tile(const GemmPhase& P, int tile) {
-    const int p = (P.nprob > 1 && tile >= P.prob[1].tile_begin) ? 1 : 0;
+// Column blocks a symmetric row block of height tm touches: j * bn <= tm i + tm - 1.
+__host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int tiles_n) {
+    const int c = (tm * i + tm - 1) / bn + 1;
+    return c < tiles_n ? c : tiles_n;
+}
+
+template <int BN, int CG>
+__device__ __forceinline__ TileInfo decode_tile(const GemmProgram& P, int tile) {
+    constexpr int TM = BM * CG;
+    int s = 0;
+    while (s + 1 < P.nphase && tile >= P.phase[s + 1].tile_begin) ++s;
+    const GemmPhaseDesc& ph = P.phase[s];
+    const int local = tile - ph.tile_begin;
+    int g = local / ph.tiles_per_matrix;
+    int t = local - g * ph.tiles_per_matrix;
+    if (ph.reverse) g = P.G - 1 - g;
+    int p = ph.prob_begin;
+    while (t >= P.prob[p].tiles_per_matrix) {
+        t -= P.prob[p].tiles_per_matrix;
+        ++p;
+    }
     const GemmProblem& pr = P.prob[p];
-    const int local = tile - pr.tile_begin;
-    const int g = local / pr.tiles_per_matrix;
-    const int t = local - g * pr.tiles_per_matrix;
     int i, j;
     if (pr.flags & kFlagSym) {
-        // Row-major enumeration of the lower triangle: t = i (i + 1) / 2 + j.
-        i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
-        while ((i + 1) * (i + 2) / 2 <= t) ++i;
-        while (i * (i + 1) / 2 > t) --i;
-        j = t - i * (i + 1) / 2;
+        int acc = 0;
+        i = 0;
+        while (true) {
+            const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n);
+            if (t < acc + cnt) break;
+            acc += cnt;
+            ++i;
+        }
+        j = t - acc;
     } else {
         i = t / pr.tiles_n;
         j = t - i * pr.tiles_n;
     }
-    return TileInfo{p, g, i * BM, j * BN};
+    return TileInfo{p, g, i * TM, j * BN, s};
 }
 
 // Address of element (row, col) of a 32 x 32 fp16 block staged with the
@@ -87,7 +123,7 @@ __device__ __forceinline__ uint32_t sw64_addr(uint32_t base, int row, int col) {
     return base + row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4) + (col & 7) * 2;
 }
 
-// fp16 sub-block row `lane` (32 values) into a 64B-swizzled staging block.
+// Row `lane` (32 values) of a 64B-swizzled fp16 block.
 __device__ __forceinline__ void stage_row_f16(uint32_t base, int lane, const float (&v)[32]) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -97,7 +133,7 @@ __device__ __forceinline__ void stage_row_f16(uint32_t base, int lane, const flo
     }
 }
 
-// fp32 sub-block row into a 128B-swizzled staging block.
+// Row `lane` of a 128B-swizzled fp32 block.
 __device__ __forceinline__ void stage_row_f32(uint32_t base, int lane, const float (&v)[32]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -107,19 +143,52 @@ __device__ __forceinline__ void stage_row_f32(uint32_t base, int lane, const flo
     }
 }
 
-// Column `lane` of the transposed block: element (j, lane) = v[j].
-__device__ __forceinline__ void stage_col_f16(uint32_t base, int lane, const float (&v)[32]) {
+// dst = src^T for a 32 x 32 fp16 block (both 64B-swizzled): 8 x 8 block (R, i)
+// of src, loaded transposed, is stored as block (i, R) of dst.
+__device__ __forceinline__ void transpose_block(uint32_t src, uint32_t dst, int lane) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const __half h = __float2half_rn(v[j]);
-        st_shared_u16(base + j * 64 + lane * 2, *reinterpret_cast<const uint16_t*>(&h));
+    for (int R = 0; R < 4; ++R) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(sw64_addr(src, 8 * R + (lane & 7), 8 * (lane >> 3)), a0, a1, a2, a3);
+        stmatrix_x4(sw64_addr(dst, lane, 8 * R), a0, a1, a2, a3);
     }
 }
 
-// Upper half of a diagonal 32 x 32 block := transpose of its lower half.
-__device__ __forceinline__ void symmetrize_block(uint32_t base, int lane) {
-    for (int j = lane + 1; j < 32; ++j)
-        st_shared_u16(sw64_addr(base, lane, j), ld_shared_u16(sw64_addr(base, j, lane)));
+// Diagonal block: row `lane` keeps its lower part (col <= lane) and takes the
+// upper part from the transposed copy, i.e. D(r, c) = D(c, r) for c > r.
+__device__ __forceinline__ void merge_upper(uint32_t d, uint32_t dt, int lane) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int c0 = 8 * k;
+        if (c0 > lane) {
+            const uint4 v = ld_shared_v4(sw64_addr(dt, lane, c0));
+            st_shared_v4(sw64_addr(d, lane, c0), v.x, v.y, v.z, v.w);
+        } else if (c0 + 7 > lane) {
+            for (int e = 0; e < 8; ++e)
+                if (c0 + e > lane) st_shared_u16(sw64_addr(d, lane, c0 + e), ld_shared_u16(sw64_addr(dt, lane, c0 + e)));
+        }
+    }
+}
+
+// Row `grow` of C, columns c0 .. c0 + 31, as 16 packed fp16 pairs.
+__device__ __forceinline__ void load_c(const GemmProblem& pr, int g, int grow, int c0, uint4 (&cb)[4]) {
+    if (grow >= pr.M) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cb[k] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const __half* crow = pr.C + static_cast<long long>(g) * pr.strideC + static_cast<long long>(grow) * pr.ldc + c0;
+    if (c0 + 32 <= pr.N) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cb[k] = *reinterpret_cast<const uint4*>(crow + 8 * k);
+    } else {
+        uint16_t h[32];
+        for (int j = 0; j < 32; ++j) h[j] = (c0 + j < pr.N) ? reinterpret_cast<const uint16_t*>(crow)[j] : 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            cb[k] = make_uint4(h[8 * k] | (uint32_t(h[8 * k + 1]) << 16), h[8 * k + 2] | (uint32_t(h[8 * k + 3]) << 16),
+                               h[8 * k + 4] | (uint32_t(h[8 * k + 5]) << 16), h[8 * k + 6] | (uint32_t(h[8 * k + 7]) << 16));
+    }
 }
 
 // Waits for an mbarrier phase during teardown, ignoring the error word.
@@ -130,21 +199,22 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmPhase P) {
-    constexpr int STAGES = Cfg<BN>::STAGES;
-    constexpr int SBUF = Cfg<BN>::SBUF;
+template <int BN, int CG>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmProgram P) {
+    constexpr int STAGES = Cfg<BN, CG>::STAGES;
+    constexpr int NCH = BN / 32;
+    constexpr int BNH = BN / CG;  // rows of B this CTA stages
     constexpr uint32_t A_BYTES = BM * BK * 2;
-    constexpr uint32_t B_BYTES = BN * BK * 2;
+    constexpr uint32_t B_BYTES = BNH * BK * 2;
     constexpr uint32_t TMEM_COLS = 2 * BN;
-    constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
+    constexpr uint32_t IDESC = idesc_f16_f32(BM * CG, BN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = sA + STAGES * A_BYTES;
     uint8_t* sEpi = sB + STAGES * B_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + 4 * 2 * SBUF);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiWarps * SBUF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
 
     const uint32_t full0 = smem_u32(bars);
@@ -156,6 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int* err = P.err;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0;  // 0 = leader of the pair
+    const int unit = blockIdx.x / CG;                        // this CTA's tile walker
+    const int units = gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -164,25 +237,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
-            mbar_init(acce0 + 8 * b, 4);
+            mbar_init(acce0 + 8 * b, kEpiWarps * CG);
         }
         mbar_init(drain_bar, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        for (int p = 0; p < P.nprob; ++p) {
-            prefetch_tmap(&P.prob[p].tmA);
-            prefetch_tmap(&P.prob[p].tmB);
-        }
+        for (int m = 0; m < P.nmaps; ++m) prefetch_tmap(&P.maps[m]);
     }
+    // Counter value at which every tile of the phases before phase s is done.
+    auto dep_target = [&](int s) { return P.phase[s].wait_tiles * (kEpiWarps * CG); };
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above overlaps the previous kernel's tail; operands written
+    // by it are read only after this point.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -190,19 +267,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
-                const TileInfo t = decode_tile<BN>(P, tile);
+            for (int tile = unit; tile < P.total_tiles && ok; tile += units) {
+                const TileInfo t = decode_tile<BN, CG>(P, tile);
                 const GemmProblem& pr = P.prob[t.p];
+                const CUtensorMap* mapA = &P.maps[pr.mA];
+                const CUtensorMap* mapB = &P.maps[pr.mB];
                 const int kblocks = (pr.K + BK - 1) / BK;
+                if (P.counters && P.phase[t.s].wait_tiles > 0) {
+                    // The operands of this phase are outputs of earlier phases on
+                    // the same matrix, stored by other CTAs.
+                    if (!wait_counter(P.counters + t.g, dep_target(t.s), err)) break;
+                    fence_proxy_async_global();
+                }
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, err)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = full0 + 8 * stage;
-                    mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-                    tma_load_3d(smem_u32(sA + stage * A_BYTES), &pr.tmA, fb, kb * BK, t.m0, t.g);
-                    tma_load_3d(smem_u32(sB + stage * B_BYTES), &pr.tmB, fb, kb * BK, t.n0, t.g);
+                    if constexpr (CG == 1) {
+                        mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+                        tma_load_3d(smem_u32(sA + stage * A_BYTES), mapA, fb, kb * BK, t.m0, t.g);
+                        tma_load_3d(smem_u32(sB + stage * B_BYTES), mapB, fb, kb * BK, t.n0, t.g);
+                    } else {
+                        // Both CTAs' halves complete on the leader's barrier.
+                        if (rank == 0) mbar_arrive_expect_tx(fb, CG * (A_BYTES + B_BYTES));
+                        const uint32_t lead_fb = map_to_rank(fb, 0);
+                        tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), mapA, lead_fb, kb * BK,
+                                         t.m0 + BM * static_cast<int>(rank), t.g);
+                        tma_load_3d_pair(smem_u32(sB + stage * B_BYTES), mapB, lead_fb, kb * BK,
+                                         t.n0 + BNH * static_cast<int>(rank), t.g);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -211,26 +306,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             }
             // The last min(issued, STAGES) loads may still be in flight; wait
-            // for each before this CTA can exit.
-            const int pending = issued < STAGES ? issued : STAGES;
-            for (int i = 0; i < pending; ++i) {
-                if (stage == 0) {
-                    stage = STAGES;
-                    phase ^= 1;
+            // for each (on the barrier that counts them) before exiting.
+            if (CG == 1 || rank == 0) {
+                const int pending = issued < STAGES ? issued : STAGES;
+                for (int i = 0; i < pending; ++i) {
+                    if (stage == 0) {
+                        stage = STAGES;
+                        phase ^= 1;
+                    }
+                    --stage;
+                    drain_wait(full0 + 8 * stage, phase);
                 }
-                --stage;
-                drain_wait(full0 + 8 * stage, phase);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------- MMA issuer (pair leader)
+        if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0;
             int iter = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x, ++iter) {
-                const TileInfo t = decode_tile<BN>(P, tile);
+            for (int tile = unit; tile < P.total_tiles && ok; tile += units, ++iter) {
+                const TileInfo t = decode_tile<BN, CG>(P, tile);
                 const GemmProblem& pr = P.prob[t.p];
                 const int kblocks = (pr.K + BK - 1) / BK;
                 const int buf = iter & 1;
@@ -247,118 +344,150 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * B_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16<CG>(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    tc_commit(empty0 + 8 * stage);
+                    if constexpr (CG == 1)
+                        tc_commit<1>(empty0 + 8 * stage);
+                    else
+                        tc_commit_pair(empty0 + 8 * stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit(accf0 + 8 * buf);
+                if constexpr (CG == 1)
+                    tc_commit<1>(accf0 + 8 * buf);
+                else
+                    tc_commit_pair(accf0 + 8 * buf);
             }
             // All MMAs issued by this thread must finish before TMEM is freed.
-            tc_commit(drain_bar);
+            tc_commit<CG>(drain_bar);
             drain_wait(drain_bar, 0);
         }
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int ew = warp - 2;
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int ew = warp - 2;                // epilogue warp 0..7
+        constexpr int CPW = NCH / 2;            // chunks per warp: two warps share a quarter
+        const int cbeg = (ew >> 2) * CPW;       // this warp's first chunk
+        const uint32_t stg = smem_u32(sEpi + ew * SBUF);
+        const uint32_t acce_lead = (CG == 2) ? map_to_rank(acce0, 0) : acce0;
         int iter = 0;
-        uint32_t groups = 0;
-        for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++iter) {
-            const TileInfo t = decode_tile<BN>(P, tile);
+        for (int tile = unit; tile < P.total_tiles; tile += units, ++iter) {
+            const TileInfo t = decode_tile<BN, CG>(P, tile);
             const GemmProblem& pr = P.prob[t.p];
             const int buf = iter & 1;
+            const int flags = pr.flags;
+            const bool sym = flags & kFlagSym;
+            const bool hasC = flags & kFlagC;
+            const bool f32 = flags & kFlagOutF32;
+            const int r0 = t.m0 + BM * static_cast<int>(rank) + q * 32;
+            const int grow = r0 + lane;
+            const bool rows_live = r0 < pr.M;
+            const int sr = r0 >> 5;
+            auto active = [&](int c) {
+                const int c0 = t.n0 + 32 * c;
+                return rows_live && c0 < pr.N && !(sym && (c0 >> 5) > sr);
+            };
+            const int cend = cbeg + CPW;
+            int c = cbeg;
+            while (c < cend && !active(c)) ++c;
+            if (hasC && P.counters && P.phase[t.s].wait_tiles > 0) {
+                // C is an earlier phase's output: acquire it like the producer.
+                if (!wait_counter(P.counters + t.g, dep_target(t.s), err)) break;
+            }
+            uint4 cb[4];
+            if (hasC && c < cend) load_c(pr, t.g, grow, t.n0 + 32 * c, cb);
+
             if (!mbar_wait(accf0 + 8 * buf, (iter >> 1) & 1, err)) break;
             tc_fence_after();
 
-            const int flags = pr.flags;
-            const bool sym = flags & kFlagSym;
-            const bool diag_tile = sym && (t.m0 == t.n0);
-            const int r0 = t.m0 + q * 32;
-            const int grow = r0 + lane;
-            const bool rows_live = r0 < pr.M;
-
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int c0 = t.n0 + c * 32;
-                if (!rows_live || c0 >= pr.N) continue;
-                if (diag_tile && c > q) continue;
-                const bool diag_block = diag_tile && (c == q);
-
+            while (c < cend) {
+                const int c0 = t.n0 + 32 * c;
                 uint32_t acc[32];
                 tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c * 32, acc);
+                int cn = c + 1;
+                while (cn < cend && !active(cn)) ++cn;
+                uint4 cbn[4];
+                if (hasC && cn < cend) load_c(pr, t.g, grow, t.n0 + 32 * cn, cbn);
                 tmem_ld_wait();
 
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = pr.alpha * __uint_as_float(acc[j]);
-                if ((flags & kFlagC) && grow < pr.M) {
-                    const __half* crow = pr.C + static_cast<long long>(t.g) * pr.strideC +
-                                         static_cast<long long>(grow) * pr.ldc + c0;
-                    if (c0 + 32 <= pr.N) {
+                if (hasC) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint4 raw = *reinterpret_cast<const uint4*>(crow + 8 * k);
-                            const __half2* h = reinterpret_cast<const __half2*>(&raw);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t w[4] = {cb[k].x, cb[k].y, cb[k].z, cb[k].w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = __half22float2(h[e]);
-                                v[8 * k + 2 * e] = fmaf(pr.beta, f.x, v[8 * k + 2 * e]);
-                                v[8 * k + 2 * e + 1] = fmaf(pr.beta, f.y, v[8 * k + 2 * e + 1]);
-                            }
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                            v[8 * k + 2 * e] = fmaf(pr.beta, f.x, v[8 * k + 2 * e]);
+                            v[8 * k + 2 * e + 1] = fmaf(pr.beta, f.y, v[8 * k + 2 * e + 1]);
                         }
-                    } else {
-                        for (int j = 0; j < 32; ++j)
-                            if (c0 + j < pr.N) v[j] = fmaf(pr.beta, __half2float(crow[j]), v[j]);
                     }
                 }
+                const bool diag_block = sym && ((c0 >> 5) == sr);
+                const bool mirror = (flags & kFlagDt) && !diag_block;
 
-                uint8_t* st = sEpi + (ew * 2 + (groups & 1)) * SBUF;
-                const uint32_t sbase = smem_u32(st);
-                if (lane == 0) bulk_wait_read<1>();
+                // The staging buffer is free once the previous sub-block's
+                // stores have read it.
+                if (lane == 0) bulk_wait_read<0>();
                 __syncwarp();
-
-                if (flags & kFlagOutF32) {
-                    stage_row_f32(sbase + kOffD, lane, v);
+                if (f32) {
+                    stage_row_f32(stg + kOffD, lane, v);
                 } else {
-                    stage_row_f16(sbase + kOffD, lane, v);
-                    if ((flags & kFlagDt) && !diag_block) stage_col_f16(sbase + kOffDt, lane, v);
+                    stage_row_f16(stg + kOffD, lane, v);
                 }
                 if (flags & kFlagD2) {
                     float v2[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v2[j] = pr.delta * v[j] + ((grow == c0 + j) ? pr.gamma : 0.0f);
-                    stage_row_f16(sbase + kOffD2, lane, v2);
-                    if ((flags & kFlagDt) && !diag_block) stage_col_f16(sbase + kOffD2t, lane, v2);
+                    for (int j = 0; j < 32; ++j) v2[j] = pr.delta * v[j] + ((grow == c0 + j) ? pr.gamma : 0.0f);
+                    stage_row_f16(stg + kOffD2, lane, v2);
                 }
-                if (diag_block) {
+                if (!f32 && (mirror || diag_block)) {
                     __syncwarp();
-                    symmetrize_block(sbase + kOffD, lane);
-                    if (flags & kFlagD2) symmetrize_block(sbase + kOffD2, lane);
+                    transpose_block(stg + kOffD, stg + kOffDt, lane);
+                    if (flags & kFlagD2) transpose_block(stg + kOffD2, stg + kOffD2t, lane);
+                    if (diag_block) {
+                        __syncwarp();
+                        merge_upper(stg + kOffD, stg + kOffDt, lane);
+                        if (flags & kFlagD2) merge_upper(stg + kOffD2, stg + kOffD2t, lane);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d(&pr.tmD, sbase + kOffD, c0, r0, t.g);
-                    if ((flags & kFlagDt) && !diag_block) tma_store_3d(&pr.tmDt, sbase + kOffDt, r0, c0, t.g);
+                    tma_store_3d(&P.maps[pr.mD], stg + kOffD, c0, r0, t.g);
+                    if (mirror) tma_store_3d(&P.maps[pr.mDt], stg + kOffDt, r0, c0, t.g);
                     if (flags & kFlagD2) {
-                        tma_store_3d(&pr.tmD2, sbase + kOffD2, c0, r0, t.g);
-                        if ((flags & kFlagDt) && !diag_block)
-                            tma_store_3d(&pr.tmD2t, sbase + kOffD2t, r0, c0, t.g);
+                        tma_store_3d(&P.maps[pr.mD2], stg + kOffD2, c0, r0, t.g);
+                        if (mirror) tma_store_3d(&P.maps[pr.mD2t], stg + kOffD2t, r0, c0, t.g);
                     }
                     bulk_commit();
                 }
-                ++groups;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cb[k] = cbn[k];
+                c = cn;
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+            if (lane == 0) {
+                if constexpr (CG == 1)
+                    mbar_arrive(acce0 + 8 * buf);
+                else
+                    mbar_arrive_cluster(acce_lead + 8 * buf);
+                if (P.counters) {
+                    // Publish this warp's part of the tile: stores complete,
+                    // then a release on the matrix's counter.
+                    bulk_wait_all();
+                    fence_proxy_async_global();
+                    red_release_add(P.counters + t.g, 1);
+                }
+            }
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -366,34 +495,67 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     tc_fence_before();
     __syncthreads();
+    // The leader's MMAs read the peer's shared memory and the peer's epilogue
+    // arrives on the leader's barriers: neither CTA leaves before both are done.
+    if constexpr (CG == 2) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, TMEM_COLS);
     }
 }
 
-template <int BN>
-int launch_impl(const GemmPhase& phase, int num_sms, cudaStream_t stream) {
+template <int BN, int CG>
+int launch_impl(const GemmProgram& prog, int num_sms, cudaStream_t stream) {
     static bool configured = false;
-    constexpr int bytes = smem_bytes<BN>();
+    constexpr int bytes = smem_bytes<BN, CG>();
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    if (phase.total_tiles <= 0) return cudaSuccess;
-    const int grid = phase.total_tiles < num_sms ? phase.total_tiles : num_sms;
-    gemm_tc_kernel<BN><<<grid, kThreads, bytes, stream>>>(phase);
-    return cudaGetLastError();
+    if (prog.total_tiles <= 0) return cudaSuccess;
+    const int units = num_sms / CG;
+    const int grid = CG * (prog.total_tiles < units ? prog.total_tiles : units);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CG;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, CG>, prog);
 }
 
 }  // namespace
 
-int gemm_smem_bytes(int bn) { return bn == 256 ? smem_bytes<256>() : smem_bytes<128>(); }
+int gemm_smem_bytes(int bn, int cg) {
+    if (cg == 2) return smem_bytes<256, 2>();
+    return bn == 256 ? smem_bytes<256, 1>() : smem_bytes<128, 1>();
+}
 
-int launch_gemm_phase(const GemmPhase& phase, int bn, int num_sms, cudaStream_t stream) {
-    if (bn == 256) return launch_impl<256>(phase, num_sms, stream);
-    return launch_impl<128>(phase, num_sms, stream);
+int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym) {
+    const int tmh = BM * cg;
+    const int tm = (M + tmh - 1) / tmh;
+    const int tn = (N + bn - 1) / bn;
+    if (!sym) return tm * tn;
+    int total = 0;
+    for (int i = 0; i < tm; ++i) total += sym_row_tiles(i, tmh, bn, tn);
+    return total;
+}
+
+int gemm_signals_per_tile(int cg) { return kEpiWarps * cg; }
+
+int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream) {
+    if (cg == 2) return launch_impl<256, 2>(prog, num_sms, stream);
+    if (bn == 256) return launch_impl<256, 1>(prog, num_sms, stream);
+    return launch_impl<128, 1>(prog, num_sms, stream);
 }
 
 }  // namespace gns
