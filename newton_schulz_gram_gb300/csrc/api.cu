@@ -219,8 +219,12 @@ int make_map(CUtensorMap* m, const Mat& x, int G, uint32_t box_c, uint32_t box_r
 }
 
 // One problem of a phase: D = alpha A B^T (+ beta C) [, D2 = delta D + gamma I].
+// A is M x K, B is N x K. An operand marked MN-major is given by its stored
+// transpose (A: K x M, B: K x N, row-major) and read through the transposed
+// descriptor, so no transposed copy is ever materialized.
 struct ProblemSpec {
     Mat A, B, D;
+    bool a_mn = false, b_mn = false;
     const Mat* C = nullptr;
     const Mat* Dt = nullptr;
     const Mat* D2 = nullptr;
@@ -323,8 +327,10 @@ class ProgramBuilder {
         return prog_.nmaps++;
     }
 
-    // A tiles are 128 rows per CTA; B tiles bn / cg rows per CTA.
-    int operand(const Mat& x, uint32_t box_rows, int& idx) {
+    // K-major: box {64 (K), rows per CTA} (A: 128, B: bn / cg). MN-major: box
+    // {64 (M or N), 64 (K)} over the stored transpose.
+    int operand(const Mat& x, uint32_t box_rows, int& idx, bool mn) {
+        (void)mn;
         idx = map_index(x, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
         return idx >= 0 ? GNS_OK : (idx == -1 ? fail(GNS_ERR_INVALID, "tensor map table full") : GNS_ERR_INVALID);
     }
@@ -337,18 +343,22 @@ class ProgramBuilder {
     int set_problem(GemmProblem& pr, const ProblemSpec& sp) {
         std::memset(&pr, 0, sizeof(pr));
         const int bn = ts_.bn, cg = ts_.cg;
-        if (sp.A.cols != sp.B.cols) return fail(GNS_ERR_INVALID, "operand K mismatch");
-        if (sp.sym && sp.A.rows != sp.B.rows) return fail(GNS_ERR_INVALID, "symmetric product must be square");
+        const int M = sp.a_mn ? sp.A.cols : sp.A.rows, Ka = sp.a_mn ? sp.A.rows : sp.A.cols;
+        const int N = sp.b_mn ? sp.B.cols : sp.B.rows, Kb = sp.b_mn ? sp.B.rows : sp.B.cols;
+        if (Ka != Kb) return fail(GNS_ERR_INVALID, "operand K mismatch");
+        if (sp.sym && M != N) return fail(GNS_ERR_INVALID, "symmetric product must be square");
         if (sp.D2 && sp.Dt && !sp.D2t) return fail(GNS_ERR_INVALID, "second output needs its transposed map");
         if (sp.D.f32 && (sp.Dt || sp.D2)) return fail(GNS_ERR_INVALID, "fp32 output supports no transposed/second output");
         if (G_ > 65535) return fail(GNS_ERR_INVALID, "too many matrices in one launch");
         pr.mA = pr.mB = pr.mD = pr.mDt = pr.mD2 = pr.mD2t = -1;
-        RET(operand(sp.A, 128, pr.mA));
-        RET(operand(sp.B, static_cast<uint32_t>(bn / cg), pr.mB));
+        RET(operand(sp.A, sp.a_mn ? 64u : 128u, pr.mA, sp.a_mn));
+        RET(operand(sp.B, sp.b_mn ? 64u : static_cast<uint32_t>(bn / cg), pr.mB, sp.b_mn));
         RET(output(sp.D, pr.mD));
         int flags = 0;
         if (sp.sym) flags |= kFlagSym;
         if (sp.D.f32) flags |= kFlagOutF32;
+        if (sp.a_mn) flags |= kFlagAmn;
+        if (sp.b_mn) flags |= kFlagBmn;
         if (sp.C) {
             flags |= kFlagC;
             pr.C = static_cast<const __half*>(sp.C->p);
@@ -368,9 +378,9 @@ class ProgramBuilder {
         pr.beta = sp.beta;
         pr.delta = sp.delta;
         pr.gamma = sp.gamma;
-        pr.M = sp.A.rows;
-        pr.N = sp.B.rows;
-        pr.K = sp.A.cols;
+        pr.M = M;
+        pr.N = N;
+        pr.K = Ka;
         pr.tiles_n = (pr.N + bn - 1) / bn;
         pr.tiles_per_matrix = gemm_tiles_per_matrix(pr.M, pr.N, bn, cg, sp.sym);
         pr.flags = flags;
@@ -448,9 +458,12 @@ BucketGeom make_geom(int R, int C) {
     return g;
 }
 
-// Workspace layout for a chunk of Gc matrices.
+// Workspace layout for a chunk of Gc matrices. The fp16 copies of X keep the
+// input's own orientation (R x C): Xa holds X0 (and the standard-NS iterates
+// alternate between Xa and Xb), Xb holds X after the restart.
 struct Layout {
-    size_t xa, xta, xb, xtb, r, z, rz, qa, qb, partial, counters, out32, o16, meta, total;
+    size_t xa, xb, r, z, rz, qa, qb, partial, counters, out32, o16, meta, total;
+    long long ld_x;
     long long ld_out32;
 };
 
@@ -462,13 +475,11 @@ Layout make_layout(const BucketGeom& g, int Gc, bool need_out32, bool need_o16, 
         off = align_up(off + bytes, 256);
         return o;
     };
-    const size_t nm = static_cast<size_t>(g.n) * g.ldm * 2 * Gc;    // X: n x m
-    const size_t mn = static_cast<size_t>(g.m) * g.ldn * 2 * Gc;    // X^T: m x n
+    L.ld_x = round_up_ll(g.C, 8);
+    const size_t xs = static_cast<size_t>(g.R) * L.ld_x * 2 * Gc;
     const size_t nn = static_cast<size_t>(g.n) * g.ldn * 2 * Gc;
-    L.xa = take(nm);
-    L.xta = take(mn);
-    L.xb = g.square ? take(nm) : 0;
-    L.xtb = take(mn);
+    L.xa = take(xs);
+    L.xb = take(xs);
     L.r = take(nn);
     L.z = take(nn);
     L.rz = g.square ? 0 : take(nn);
@@ -501,37 +512,36 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
              int restart_at, const Coeffs& cf, const OutSpec& os, cudaStream_t s) {
     ProgramBuilder prog(st, Gc, choose_tile(g.n), reinterpret_cast<int*>(st.ws + L.counters), s);
     char* ws = st.ws;
-    const int n = g.n, m = g.m;
-    Mat Xa = mat16(ws, L.xa, n, m, g.ldm);
-    Mat XTa = mat16(ws, L.xta, m, n, g.ldn);
-    Mat XTb = mat16(ws, L.xtb, m, n, g.ldn);
-    // Scale + cast: the input (R x C) is written directly and transposed.
-    {
-        const Mat& direct = g.transposed ? XTa : Xa;
-        const Mat& trans = g.transposed ? Xa : XTa;
-        LAUNCH(kClsCast, launch_scale_cast(in, Gc, g.R, g.C, reinterpret_cast<const float*>(ws + L.partial), nblk, g.k_exp,
-                             direct.p, direct.ld, direct.stride, trans.p, trans.ld, trans.stride, st.err, s));
-    }
+    const int n = g.n;
+    // Stored copies of X in the input's orientation (R x C).
+    Mat Xa = mat16(ws, L.xa, g.R, g.C, L.ld_x);
+    Mat Xb = mat16(ws, L.xb, g.R, g.C, L.ld_x);
+    LAUNCH(kClsCast, launch_scale_cast(in, Gc, g.R, g.C, reinterpret_cast<const float*>(ws + L.partial), nblk, g.k_exp,
+                                       Xa.p, Xa.ld, Xa.stride, st.err, s));
     const float inv_s = 1.0f / g.s;
     const float out_scale = std::ldexp(1.0f, -g.k_exp);
-    // Consecutive phases visit the matrices in opposite orders, so each phase
-    // starts on the matrices the previous one wrote last (still in L2).
-    int phase_no = 0;
-    auto phase = [&](const ProblemSpec& p0, const ProblemSpec* p1) {
-        return prog.phase(p0, p1, (phase_no++ & 1) != 0);
+    // Operand views of the stored X (Xs = X when R <= C, Xs = X^T when R > C):
+    // X as an n-row operand (K = m) and X^T as an m-row operand (K = n).
+    auto x_rows = [&](ProblemSpec& p, bool as_a, const Mat& xs) {
+        (as_a ? p.A : p.B) = xs;
+        (as_a ? p.a_mn : p.b_mn) = g.transposed;
     };
+    auto xt_rows = [&](ProblemSpec& p, bool as_a, const Mat& xs) {
+        (as_a ? p.A : p.B) = xs;
+        (as_a ? p.a_mn : p.b_mn) = !g.transposed;
+    };
+    auto phase = [&](const ProblemSpec& p0, const ProblemSpec* p1) { return prog.phase(p0, p1, false); };
 
     if (g.square) {
         // Dion3 Algorithm 1 with symmetric A = X X^T and B = b A + c A^2
         // (App. C.3): X <- a X + B X, the last step writing the output.
-        Mat Xb = mat16(ws, L.xb, n, n, g.ldn);
         Mat A = mat16(ws, L.r, n, n, g.ldn);
         Mat B = mat16(ws, L.z, n, n, g.ldn);
-        Mat X = Xa, XT = XTa, Xn = Xb, XTn = XTb;
+        Mat X = Xa, Xn = Xb;
         for (int t = 0; t < steps; ++t) {
             ProblemSpec pa;
-            pa.A = X;
-            pa.B = X;
+            x_rows(pa, true, X);
+            x_rows(pa, false, X);
             pa.D = A;
             pa.Dt = &A;
             pa.sym = true;
@@ -546,18 +556,17 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             pb.beta = cf.b[t];
             pb.sym = true;
             RET(phase(pb, nullptr));
+            // X' = B X + a X: B is symmetric, X enters as the N x K operand X^T.
             ProblemSpec px;
             px.A = B;
-            px.B = XT;
+            xt_rows(px, false, X);
             px.C = &X;
             if (t + 1 < steps) {
                 px.D = Xn;
-                px.Dt = &XTn;
                 px.alpha = inv_s;
                 px.beta = cf.a[t];
                 RET(phase(px, nullptr));
                 std::swap(X, Xn);
-                std::swap(XT, XTn);
             } else {
                 px.D = os.out;
                 px.alpha = inv_s * out_scale;
@@ -574,30 +583,38 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     Mat RZ = mat16(ws, L.rz, n, n, g.ldn);
     Mat Qc = mat16(ws, L.qa, n, n, g.ldn);
     Mat Qn = mat16(ws, L.qb, n, n, g.ldn);
-    Mat X = Xa, XT = XTa, XTn = XTb;
+    Mat X = Xa, Xn = Xb;
 
     auto gram = [&](void) -> int {
         ProblemSpec p;
-        p.A = X;
-        p.B = X;
+        x_rows(p, true, X);
+        x_rows(p, false, X);
         p.D = R;
         p.Dt = &R;
         p.sym = true;
         return phase(p, nullptr);
+    };
+    // Q X in the stored orientation: Q X (R <= C) or X^T Q = (Q X)^T (R > C).
+    auto qx = [&](ProblemSpec& p) {
+        if (!g.transposed) {
+            p.A = Qc;
+            xt_rows(p, false, X);
+        } else {
+            xt_rows(p, true, X);
+            p.B = Qc;
+        }
     };
     RET(gram());
     bool q_identity = true;
     for (int t = 1; t <= steps; ++t) {
         const float a = cf.a[t - 1], b = cf.b[t - 1], c = cf.c[t - 1];
         if (is_restart_after(t - 1, steps, restart_at)) {
-            // X <- Q X (n x m) and its transpose, then R <- X X^T, Q <- I.
+            // X <- Q X, then R <- X X^T, Q <- I.
             ProblemSpec p;
-            p.A = Qc;
-            p.B = XT;
-            p.D = X;  // X is not read by this phase
-            p.Dt = &XTn;
+            qx(p);
+            p.D = Xn;
             RET(phase(p, nullptr));
-            std::swap(XT, XTn);
+            std::swap(X, Xn);
             RET(gram());
             q_identity = true;
         }
@@ -666,13 +683,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     }
     // O = Q X, written in the caller's orientation.
     ProblemSpec p;
-    if (!g.transposed) {
-        p.A = Qc;
-        p.B = XT;
-    } else {
-        p.A = XT;
-        p.B = Qc;
-    }
+    qx(p);
     p.D = os.out;
     p.alpha = out_scale;
     RET(phase(p, nullptr));

@@ -107,19 +107,15 @@ __global__ void __launch_bounds__(kThreads) sumsq_kernel(MatrixSet in, long long
     if (threadIdx.x == 0) partial[static_cast<long long>(blockIdx.y) * nblk + blockIdx.x] = t;
 }
 
-// 64 x 64 tiles; each block scales, casts and writes the tile directly and
-// transposed (through shared memory).
-constexpr int TILE = 64;
-
+// Scale and cast, in the input's own layout: 4 consecutive elements per
+// thread (vector load and store when aligned), grid-stride over the matrix.
 __global__ void __launch_bounds__(kThreads) scale_cast_kernel(MatrixSet in, int R, int C, const float* partial,
-                                                              int nblk, int k_exp, __half* direct,
-                                                              long long ld_d, long long stride_d, __half* trans,
-                                                              long long ld_t, long long stride_t, int* err) {
-    __shared__ float tile[TILE][TILE + 1];
+                                                              int nblk, int k_exp, __half* out, long long ld_o,
+                                                              long long stride_o, int* err) {
     __shared__ float s_scale;
     grid_dependency_wait();
     grid_launch_dependents();
-    const int g = blockIdx.z;
+    const int g = blockIdx.y;
     if (threadIdx.x == 0) {
         float t = 0.0f;
         const float* p = partial + static_cast<long long>(g) * nblk;
@@ -131,67 +127,35 @@ __global__ void __launch_bounds__(kThreads) scale_cast_kernel(MatrixSet in, int 
     __syncthreads();
     const float scale = s_scale;
     const float* x = mat_f32(in, g);
-    const int r0 = blockIdx.y * TILE, c0 = blockIdx.x * TILE;
-    __half* dg = direct + static_cast<long long>(g) * stride_d;
-    __half* tg = trans + static_cast<long long>(g) * stride_t;
-
-    // Read + direct write: 16 threads per row, 4 consecutive columns each.
-    const int tr = threadIdx.x / 16, tc = (threadIdx.x % 16) * 4;
-    const bool vec_in = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && (C % 4 == 0);
-#pragma unroll
-    for (int pass = 0; pass < TILE / 16; ++pass) {
-        const int r = r0 + pass * 16 + tr;
-        const int c = c0 + tc;
+    __half* og = out + static_cast<long long>(g) * stride_o;
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && (C % 4 == 0);
+    const long long groups_per_row = (C + 3) / 4;
+    const long long groups = static_cast<long long>(R) * groups_per_row;
+    for (long long q = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; q < groups;
+         q += static_cast<long long>(gridDim.x) * kThreads) {
+        const long long r = q / groups_per_row;
+        const int c = static_cast<int>(q - r * groups_per_row) * 4;
+        const float* src = x + r * C + c;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (r < R) {
-            const float* src = x + static_cast<long long>(r) * C + c;
-            if (vec_in && c + 3 < C) {
-                const float4 f = *reinterpret_cast<const float4*>(src);
-                v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-            } else {
-                for (int e = 0; e < 4; ++e)
-                    if (c + e < C) v[e] = src[e];
-            }
-            for (int e = 0; e < 4; ++e) v[e] *= scale;
-            __half* dst = dg + static_cast<long long>(r) * ld_d + c;
-            if (c + 3 < C) {
-                // ld_d is a multiple of 8 halves, c a multiple of 4: 8-byte aligned.
-                __half2 h01 = __floats2half2_rn(v[0], v[1]);
-                __half2 h23 = __floats2half2_rn(v[2], v[3]);
-                uint2 packed;
-                packed.x = *reinterpret_cast<uint32_t*>(&h01);
-                packed.y = *reinterpret_cast<uint32_t*>(&h23);
-                *reinterpret_cast<uint2*>(dst) = packed;
-            } else {
-                for (int e = 0; e < 4; ++e)
-                    if (c + e < C) dst[e] = __float2half_rn(v[e]);
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) tile[pass * 16 + tr][tc + e] = v[e];
-    }
-    __syncthreads();
-    // Transposed write: output row = input column, 16 threads per row.
-#pragma unroll
-    for (int pass = 0; pass < TILE / 16; ++pass) {
-        const int oc = pass * 16 + tr;  // column of the input tile = row of the output
-        const int orow = c0 + oc;
-        if (orow >= C) continue;
-        const int ocol = r0 + tc;       // 4 input rows
-        __half* dst = tg + static_cast<long long>(orow) * ld_t + ocol;
-        float v[4];
-        for (int e = 0; e < 4; ++e) v[e] = tile[tc + e][oc];
-        if (ocol + 3 < R) {
-            __half2 h01 = __floats2half2_rn(v[0], v[1]);
-            __half2 h23 = __floats2half2_rn(v[2], v[3]);
-            uint2 packed;
-            packed.x = *reinterpret_cast<uint32_t*>(&h01);
-            packed.y = *reinterpret_cast<uint32_t*>(&h23);
-            *reinterpret_cast<uint2*>(dst) = packed;
+        if (vec) {
+            const float4 f = *reinterpret_cast<const float4*>(src);
+            v[0] = f.x;
+            v[1] = f.y;
+            v[2] = f.z;
+            v[3] = f.w;
         } else {
             for (int e = 0; e < 4; ++e)
-                if (ocol + e < R) dst[e] = __float2half_rn(v[e]);
+                if (c + e < C) v[e] = src[e];
         }
+        __half* dst = og + r * ld_o + c;
+        // ld_o is a multiple of 8 halves and c of 4: 8-byte aligned; columns
+        // past C land in the row padding.
+        __half2 h01 = __floats2half2_rn(v[0] * scale, v[1] * scale);
+        __half2 h23 = __floats2half2_rn(v[2] * scale, v[3] * scale);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&h01);
+        packed.y = *reinterpret_cast<uint32_t*>(&h23);
+        *reinterpret_cast<uint2*>(dst) = packed;
     }
 }
 
@@ -364,14 +328,12 @@ int launch_sumsq(const MatrixSet& in, long long numel, int G, float* partial, in
     return launch_pdl(sumsq_kernel, dim3(nblk, G), dim3(kThreads), s, in, numel, nblk, partial);
 }
 
-int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* partial, int nblk, int k_exp,
-                      void* direct, long long ld_direct, long long stride_direct, void* trans, long long ld_trans,
-                      long long stride_trans, int* err, cudaStream_t s) {
+int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* partial, int nblk, int k_exp, void* out,
+                      long long ld_out, long long stride_out, int* err, cudaStream_t s) {
     if (G <= 0) return cudaSuccess;
-    dim3 grid((C + TILE - 1) / TILE, (R + TILE - 1) / TILE, G);
-    return launch_pdl(scale_cast_kernel, grid, dim3(kThreads), s, in, R, C, partial, nblk, k_exp,
-                      static_cast<__half*>(direct), ld_direct, stride_direct, static_cast<__half*>(trans), ld_trans,
-                      stride_trans, err);
+    const long long groups = static_cast<long long>(R) * ((C + 3) / 4);
+    return launch_pdl(scale_cast_kernel, dim3(grid_for(groups, kThreads * 8), G), dim3(kThreads), s, in, R, C, partial,
+                      nblk, k_exp, static_cast<__half*>(out), ld_out, stride_out, err);
 }
 
 int launch_copy_rows_f32(const float* in, long long ld_in, long long stride_in, float* out, int G, int R, int C,

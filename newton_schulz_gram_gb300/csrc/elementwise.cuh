@@ -22,15 +22,12 @@ int norm_blocks(long long numel);
 int launch_sumsq(const MatrixSet& in, long long numel, int G, float* partial, int* err,
                  cudaStream_t s);
 
-// Scale and cast an fp32 R x C matrix set to fp16:
+// Scale and cast an fp32 R x C matrix set to fp16 in the same layout:
 //   scale_g = 2^k / (1.05 * (sqrt(sum_b partial[g][b]) + 1e-7)),
-//   direct[g] (R x C, row stride ld_direct) = fp16(scale_g * x),
-//   trans[g] (C x R, row stride ld_trans) = its transpose.
+//   out[g] (R x C, row stride ld_out, a multiple of 8) = fp16(scale_g * x).
 // A non-finite norm raises the non-finite error word.
-int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* partial, int nblk,
-                      int k_exp, void* direct, long long ld_direct, long long stride_direct,
-                      void* trans, long long ld_trans, long long stride_trans, int* err,
-                      cudaStream_t s);
+int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* partial, int nblk, int k_exp, void* out,
+                      long long ld_out, long long stride_out, int* err, cudaStream_t s);
 
 // out[g] (R x C, contiguous) = in[g] (R x C, row stride ld_in), fp32.
 int launch_copy_rows_f32(const float* in, long long ld_in, long long stride_in, float* out, int G,

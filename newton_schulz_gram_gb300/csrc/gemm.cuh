@@ -26,7 +26,9 @@ enum GemmFlags : int {
     kFlagC = 2,       // add beta * C (fp16, row-major, same shape as D)
     kFlagDt = 4,      // also write D transposed into Dt ([G][N][M])
     kFlagD2 = 8,      // also write D2 = delta * D + gamma * I (fp16), and its mirror D2t
-    kFlagOutF32 = 16  // D is fp32 (otherwise fp16)
+    kFlagOutF32 = 16, // D is fp32 (otherwise fp16)
+    kFlagAmn = 32,    // A is MN-major: the stored matrix is K x M (A^T row-major)
+    kFlagBmn = 64     // B is MN-major: the stored matrix is K x N (B^T row-major)
 };
 
 constexpr int kMaxMaps = 24;
@@ -41,9 +43,10 @@ struct GemmProblem {
     int M, N, K;
     int tiles_n, tiles_per_matrix;
     int flags;
-    // Indices into GemmProgram::maps (-1 when unused). Operand maps: box
-    // {64, 128}, 128-byte swizzle. Output maps: box {32, 32}, 64-byte swizzle
-    // (fp16) or 128-byte swizzle (fp32).
+    // Indices into GemmProgram::maps (-1 when unused). K-major operand maps:
+    // box {64 (K), rows per CTA}; MN-major operand maps: box {64 (M or N),
+    // 64 (K)}; both 128-byte swizzle. Output maps: box {32, 32}, 64-byte
+    // swizzle (fp16) or 128-byte swizzle (fp32).
     int mA, mB, mD, mDt, mD2, mD2t;
 };
 

@@ -117,6 +117,30 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmProgram& P, int tile) 
     return TileInfo{p, g, i * TM, j * BN, s};
 }
 
+// An MN-major operand tile is staged as 64-wide M/N blocks of 64 K rows
+// (one TMA box each), 8 KB apart.
+constexpr uint32_t kMnBlockBytes = 64 * BK * 2;
+
+// One k-block of one operand into shared memory: a K-major tile is one box
+// {64 (K), rows}; an MN-major tile is rows / 64 boxes {64 (M or N), 64 (K)}.
+template <int CG>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn, int row0,
+                                             int rows, int kb, int g) {
+    if (!mn) {
+        if constexpr (CG == 1)
+            tma_load_3d(dst, map, bar, kb * BK, row0, g);
+        else
+            tma_load_3d_pair(dst, map, bar, kb * BK, row0, g);
+    } else {
+        for (int h = 0; h < rows / 64; ++h) {
+            if constexpr (CG == 1)
+                tma_load_3d(dst + h * kMnBlockBytes, map, bar, row0 + 64 * h, kb * BK, g);
+            else
+                tma_load_3d_pair(dst + h * kMnBlockBytes, map, bar, row0 + 64 * h, kb * BK, g);
+        }
+    }
+}
+
 // Address of element (row, col) of a 32 x 32 fp16 block staged with the
 // 64-byte swizzle (16-byte chunk index XOR (row / 2) mod 4).
 __device__ __forceinline__ uint32_t sw64_addr(uint32_t base, int row, int col) {
@@ -207,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     constexpr uint32_t A_BYTES = BM * BK * 2;
     constexpr uint32_t B_BYTES = BNH * BK * 2;
     constexpr uint32_t TMEM_COLS = 2 * BN;
-    constexpr uint32_t IDESC = idesc_f16_f32(BM * CG, BN);
+    constexpr uint32_t IDESC = idesc_f16_f32(BM * CG, BN);  // K-major; MN-major bits added per problem
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -272,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const GemmProblem& pr = P.prob[t.p];
                 const CUtensorMap* mapA = &P.maps[pr.mA];
                 const CUtensorMap* mapB = &P.maps[pr.mB];
+                const bool a_mn = pr.flags & kFlagAmn;
+                const bool b_mn = pr.flags & kFlagBmn;
                 const int kblocks = (pr.K + BK - 1) / BK;
                 if (P.counters && P.phase[t.s].wait_tiles > 0) {
                     // The operands of this phase are outputs of earlier phases on
@@ -285,19 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     const uint32_t fb = full0 + 8 * stage;
-                    if constexpr (CG == 1) {
-                        mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-                        tma_load_3d(smem_u32(sA + stage * A_BYTES), mapA, fb, kb * BK, t.m0, t.g);
-                        tma_load_3d(smem_u32(sB + stage * B_BYTES), mapB, fb, kb * BK, t.n0, t.g);
-                    } else {
-                        // Both CTAs' halves complete on the leader's barrier.
-                        if (rank == 0) mbar_arrive_expect_tx(fb, CG * (A_BYTES + B_BYTES));
-                        const uint32_t lead_fb = map_to_rank(fb, 0);
-                        tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), mapA, lead_fb, kb * BK,
-                                         t.m0 + BM * static_cast<int>(rank), t.g);
-                        tma_load_3d_pair(smem_u32(sB + stage * B_BYTES), mapB, lead_fb, kb * BK,
-                                         t.n0 + BNH * static_cast<int>(rank), t.g);
-                    }
+                    // With CG == 2 both CTAs' halves complete on the leader's barrier.
+                    if (CG == 1 || rank == 0) mbar_arrive_expect_tx(fb, CG * (A_BYTES + B_BYTES));
+                    const uint32_t bar = (CG == 2) ? map_to_rank(fb, 0) : fb;
+                    const int arow = t.m0 + BM * static_cast<int>(rank);
+                    const int brow = t.n0 + BNH * static_cast<int>(rank);
+                    load_operand<CG>(smem_u32(sA + stage * A_BYTES), mapA, bar, a_mn, arow, BM, kb, t.g);
+                    load_operand<CG>(smem_u32(sB + stage * B_BYTES), mapB, bar, b_mn, brow, BNH, kb, t.g);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -331,6 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const GemmProblem& pr = P.prob[t.p];
                 const int kblocks = (pr.K + BK - 1) / BK;
                 const int buf = iter & 1;
+                const uint32_t a_mn = (pr.flags & kFlagAmn) ? 1u : 0u;
+                const uint32_t b_mn = (pr.flags & kFlagBmn) ? 1u : 0u;
+                const uint32_t idesc = IDESC | (a_mn << 15) | (b_mn << 16);
+                // Per 16-wide k step: 32 bytes along a K-major row, or two
+                // 8-row groups (2048 bytes) of an MN-major tile.
+                const uint32_t a_step = a_mn ? (2048 >> 4) : (32 >> 4);
+                const uint32_t b_step = b_mn ? (2048 >> 4) : (32 >> 4);
                 if (!mbar_wait(acce0 + 8 * buf, ((iter >> 1) & 1) ^ 1, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
@@ -340,11 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * A_BYTES));
-                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * B_BYTES));
+                    const uint32_t sa = smem_u32(sA + stage * A_BYTES);
+                    const uint32_t sb = smem_u32(sB + stage * B_BYTES);
+                    const uint64_t adesc = a_mn ? sw128_mnmajor_desc(sa, kMnBlockBytes) : sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = b_mn ? sw128_mnmajor_desc(sb, kMnBlockBytes) : sw128_kmajor_desc(sb);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_f16<CG>(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16<CG>(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc,
+                                       (kb | kk) != 0 ? 1u : 0u);
                     }
                     if constexpr (CG == 1)
                         tc_commit<1>(empty0 + 8 * stage);

@@ -271,12 +271,27 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B (K-major),
-// fp32 accumulator, M x N tile.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+// Shared-memory matrix descriptor for an MN-major operand staged by TMA loads
+// of 64 (M or N) x 64 (K) boxes with 128-byte swizzle: each K row is 128
+// bytes (64 fp16 along M/N), 8-row K groups are 1024 bytes apart (stride byte
+// offset) and consecutive 64-wide M/N blocks are `mn_block_bytes` apart
+// (leading byte offset). The tile base must be 1024-byte aligned.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);        // start address
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                     // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                             // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B, fp32
+// accumulator, M x N tile; a_mn / b_mn select MN-major (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, uint32_t a_mn = 0, uint32_t b_mn = 0) {
     return (1u << 4)                                 // D format: f32
            | (0u << 7) | (0u << 10)                  // A, B format: f16
-           | (0u << 15) | (0u << 16)                 // A, B K-major
+           | (a_mn << 15) | (b_mn << 16)             // A, B major-ness (0 = K-major)
            | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
