@@ -234,22 +234,31 @@ struct ProblemSpec {
     bool reverse = false;  // visit matrices last to first (starts on L2-resident data)
 };
 
-// Tile shape for a program: 256 x 256 tiles on CTA pairs when the matrices
-// fill them, else 128 x 128 tiles on single CTAs. GNS_TILE=128x1|256x1|256x2
-// forces one shape (tuning).
+// Tile shape for a program: 256 x 256 tiles on CTA pairs, two pairs per
+// cluster, when the matrices fill them; else 128 x 128 tiles on single CTAs.
+// GNS_TILE=128x1|256x1|256x2|256x2x2 forces one shape (tuning). With two
+// pairs per cluster, non-symmetric products share their A operand between
+// the pairs (multicast); symmetric ones only when GNS_SHARE_SYM=1 (their
+// rows must then be padded to an even tile count).
 struct TileShape {
-    int bn, cg;
+    int bn, cg, np;
 };
 
 TileShape choose_tile(int n) {
     const char* force = std::getenv("GNS_TILE");
     if (force) {
         const std::string f(force);
-        if (f == "128x1") return {128, 1};
-        if (f == "256x1") return {256, 1};
-        if (f == "256x2") return {256, 2};
+        if (f == "128x1") return {128, 1, 1};
+        if (f == "256x1") return {256, 1, 1};
+        if (f == "256x2") return {256, 2, 1};
+        if (f == "256x2x2") return {256, 2, 2};
     }
-    return n >= 192 ? TileShape{256, 2} : TileShape{128, 1};
+    return n >= 192 ? TileShape{256, 2, 2} : TileShape{128, 1, 1};
+}
+
+bool share_symmetric() {
+    const char* e = std::getenv("GNS_SHARE_SYM");
+    return e && std::atoi(e) != 0;
 }
 
 // Collects the phases of one launch. Tensor maps are shared between the
@@ -302,7 +311,7 @@ class ProgramBuilder {
         prog_.err = st_.err;
         prog_.G = G_;
         cudaStream_t s = s_;
-        LAUNCH(kClsGemm, launch_gemm_program(prog_, ts_.bn, ts_.cg, st_.num_sms, s));
+        LAUNCH(kClsGemm, launch_gemm_program(prog_, ts_.bn, ts_.cg, ts_.np, st_.num_sms, s));
         reset();
         return GNS_OK;
     }
@@ -359,6 +368,8 @@ class ProgramBuilder {
         if (sp.D.f32) flags |= kFlagOutF32;
         if (sp.a_mn) flags |= kFlagAmn;
         if (sp.b_mn) flags |= kFlagBmn;
+        const bool share = ts_.np == 2 && (!sp.sym || share_symmetric());
+        if (share) flags |= kFlagShareA;
         if (sp.C) {
             flags |= kFlagC;
             pr.C = static_cast<const __half*>(sp.C->p);
@@ -382,7 +393,7 @@ class ProgramBuilder {
         pr.N = N;
         pr.K = Ka;
         pr.tiles_n = (pr.N + bn - 1) / bn;
-        pr.tiles_per_matrix = gemm_tiles_per_matrix(pr.M, pr.N, bn, cg, sp.sym);
+        pr.tiles_per_matrix = gemm_tiles_per_matrix(pr.M, pr.N, bn, cg, sp.sym, ts_.np, share, &pr.tiles_n_walk);
         pr.flags = flags;
         return GNS_OK;
     }

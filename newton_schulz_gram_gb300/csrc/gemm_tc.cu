@@ -40,13 +40,12 @@ static_assert(sizeof(GemmProgram) <= 32764, "kernel parameter block too large");
 constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 
-// One per-warp epilogue staging buffer (bytes): four 32 x 32 fp16 blocks, or
-// one 32 x 32 fp32 block at kOffD.
-constexpr int SBUF = 8192;
+// One per-warp epilogue staging buffer (bytes): a 32 x 32 fp16 block and its
+// transpose, or one 32 x 32 fp32 block. A second output reuses it in a
+// second pass.
+constexpr int SBUF = 4096;
 constexpr int kOffD = 0;
 constexpr int kOffDt = 2048;
-constexpr int kOffD2 = 4096;
-constexpr int kOffD2t = 6144;
 
 // Kernel variants: <BN, CG>. CG = 1: one CTA computes a 128 x BN tile.
 // CG = 2: a cluster of two CTAs computes a 256 x BN tile with paired MMAs
@@ -56,15 +55,15 @@ template <int BN, int CG>
 struct Cfg;
 template <>
 struct Cfg<128, 1> {
-    static constexpr int STAGES = 5;
+    static constexpr int STAGES = 6;
 };
 template <>
 struct Cfg<256, 1> {
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = 4;
 };
 template <>
 struct Cfg<256, 2> {
-    static constexpr int STAGES = 5;
+    static constexpr int STAGES = 6;
 };
 
 template <int BN, int CG>
@@ -77,10 +76,12 @@ struct TileInfo {
     int p, g, m0, n0, s;  // problem, matrix, tile origin, phase
 };
 
-// Column blocks a symmetric row block of height tm touches: j * bn <= tm i + tm - 1.
-__host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int tiles_n) {
-    const int c = (tm * i + tm - 1) / bn + 1;
-    return c < tiles_n ? c : tiles_n;
+// Column blocks a symmetric row block of height tm touches: j * bn <= tm i + tm - 1
+// (rounded up to even when two CTA pairs share the row's A).
+__host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int tiles_n, bool share) {
+    int c = (tm * i + tm - 1) / bn + 1;
+    c = c < tiles_n ? c : tiles_n;
+    return share ? c + (c & 1) : c;
 }
 
 template <int BN, int CG>
@@ -100,19 +101,22 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmProgram& P, int tile) 
     }
     const GemmProblem& pr = P.prob[p];
     int i, j;
+    // Tiles past the real ones (padding) decode to out-of-range tiles: their
+    // loads read zeros and their epilogue writes nothing.
     if (pr.flags & kFlagSym) {
+        const bool share = pr.flags & kFlagShareA;
         int acc = 0;
         i = 0;
         while (true) {
-            const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n);
+            const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n, share);
             if (t < acc + cnt) break;
             acc += cnt;
             ++i;
         }
         j = t - acc;
     } else {
-        i = t / pr.tiles_n;
-        j = t - i * pr.tiles_n;
+        i = t / pr.tiles_n_walk;
+        j = t - i * pr.tiles_n_walk;
     }
     return TileInfo{p, g, i * TM, j * BN, s};
 }
@@ -123,21 +127,22 @@ constexpr uint32_t kMnBlockBytes = 64 * BK * 2;
 
 // One k-block of one operand into shared memory: a K-major tile is one box
 // {64 (K), rows}; an MN-major tile is rows / 64 boxes {64 (M or N), 64 (K)}.
-template <int CG>
-__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn, int row0,
-                                             int rows, int kb, int g) {
-    if (!mn) {
-        if constexpr (CG == 1)
-            tma_load_3d(dst, map, bar, kb * BK, row0, g);
+// mode 0: this CTA's own barrier; 1: the pair leader's barrier (bar is a
+// cluster address); 2: multicast to the CTAs in `mask`, completing on the
+// pair leader's barrier of each destination.
+__device__ __forceinline__ void load_operand(int mode, uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn,
+                                             int row0, int rows, int kb, int g, uint16_t mask) {
+    const int boxes = mn ? rows / 64 : 1;
+    for (int h = 0; h < boxes; ++h) {
+        const uint32_t d = dst + h * kMnBlockBytes;
+        const int c0 = mn ? row0 + 64 * h : kb * BK;
+        const int c1 = mn ? kb * BK : row0;
+        if (mode == 0)
+            tma_load_3d(d, map, bar, c0, c1, g);
+        else if (mode == 1)
+            tma_load_3d_pair(d, map, bar, c0, c1, g);
         else
-            tma_load_3d_pair(dst, map, bar, kb * BK, row0, g);
-    } else {
-        for (int h = 0; h < rows / 64; ++h) {
-            if constexpr (CG == 1)
-                tma_load_3d(dst + h * kMnBlockBytes, map, bar, row0 + 64 * h, kb * BK, g);
-            else
-                tma_load_3d_pair(dst + h * kMnBlockBytes, map, bar, row0 + 64 * h, kb * BK, g);
-        }
+            tma_load_3d_multicast_pair(d, map, bar, c0, c1, g, mask);
     }
 }
 
@@ -223,8 +228,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-template <int BN, int CG>
+template <int BN, int CG, int NP>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmProgram P) {
+    static_assert(NP == 1 || CG == 2, "pairs per cluster needs paired MMAs");
+    constexpr int CL = CG * NP;  // CTAs per cluster
     constexpr int STAGES = Cfg<BN, CG>::STAGES;
     constexpr int NCH = BN / 32;
     constexpr int BNH = BN / CG;  // rows of B this CTA stages
@@ -250,14 +257,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int* err = P.err;
-    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0;  // 0 = leader of the pair
-    const int unit = blockIdx.x / CG;                        // this CTA's tile walker
-    const int units = gridDim.x / CG;
+    const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0;  // rank in the cluster
+    const uint32_t rank = crank & (CG - 1);                  // rank in the pair: 0 = leader
+    const uint32_t lead = crank & ~uint32_t(CG - 1);         // cluster rank of the pair leader
+    const int pair = static_cast<int>(crank >> 1) & (NP - 1);  // pair within the cluster
+    const int unit = blockIdx.x / CL;                        // this cluster's tile walker
+    const int units = gridDim.x / CL;
+    const int nwalk = P.total_tiles / NP;                    // super-tiles: NP consecutive tiles
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
+            // With two pairs per cluster every stage is released by both
+            // pairs' MMAs (a shared A half lands in both pairs).
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, NP);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers exist before any remote use
+    if constexpr (CL > 1) cluster_sync();  // all CTAs' barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // Everything above overlaps the previous kernel's tail; operands written
@@ -291,13 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int tile = unit; tile < P.total_tiles && ok; tile += units) {
-                const TileInfo t = decode_tile<BN, CG>(P, tile);
+            for (int w = unit; w < nwalk && ok; w += units) {
+                const TileInfo t = decode_tile<BN, CG>(P, w * NP + pair);
                 const GemmProblem& pr = P.prob[t.p];
                 const CUtensorMap* mapA = &P.maps[pr.mA];
                 const CUtensorMap* mapB = &P.maps[pr.mB];
                 const bool a_mn = pr.flags & kFlagAmn;
                 const bool b_mn = pr.flags & kFlagBmn;
+                const bool share = (NP == 2) && (pr.flags & kFlagShareA);
                 const int kblocks = (pr.K + BK - 1) / BK;
                 if (P.counters && P.phase[t.s].wait_tiles > 0) {
                     // The operands of this phase are outputs of earlier phases on
@@ -311,13 +325,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     const uint32_t fb = full0 + 8 * stage;
-                    // With CG == 2 both CTAs' halves complete on the leader's barrier.
-                    if (CG == 1 || rank == 0) mbar_arrive_expect_tx(fb, CG * (A_BYTES + B_BYTES));
-                    const uint32_t bar = (CG == 2) ? map_to_rank(fb, 0) : fb;
                     const int arow = t.m0 + BM * static_cast<int>(rank);
                     const int brow = t.n0 + BNH * static_cast<int>(rank);
-                    load_operand<CG>(smem_u32(sA + stage * A_BYTES), mapA, bar, a_mn, arow, BM, kb, t.g);
-                    load_operand<CG>(smem_u32(sB + stage * B_BYTES), mapB, bar, b_mn, brow, BNH, kb, t.g);
+                    if constexpr (CG == 1) {
+                        mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+                        load_operand(0, smem_u32(sA + stage * A_BYTES), mapA, fb, a_mn, arow, BM, kb, t.g, 0);
+                        load_operand(0, smem_u32(sB + stage * B_BYTES), mapB, fb, b_mn, brow, BNH, kb, t.g, 0);
+                    } else {
+                        // All halves complete on the pair leader's barrier. A
+                        // shared A half is loaded once by the first pair and
+                        // multicast to the same-rank CTA of both pairs.
+                        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (A_BYTES + B_BYTES));
+                        const uint32_t lead_fb = map_to_rank(fb, lead);
+                        if (!share) {
+                            load_operand(1, smem_u32(sA + stage * A_BYTES), mapA, lead_fb, a_mn, arow, BM, kb, t.g, 0);
+                        } else if (pair == 0) {
+                            const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2 + rank)));
+                            load_operand(2, smem_u32(sA + stage * A_BYTES), mapA, lead_fb, a_mn, arow, BM, kb, t.g,
+                                         mask);
+                        }
+                        load_operand(1, smem_u32(sB + stage * B_BYTES), mapB, lead_fb, b_mn, brow, BNH, kb, t.g, 0);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -346,8 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int iter = 0;
             bool ok = true;
-            for (int tile = unit; tile < P.total_tiles && ok; tile += units, ++iter) {
-                const TileInfo t = decode_tile<BN, CG>(P, tile);
+            constexpr uint16_t kStageMask = (NP == 2) ? 0xF : 0x3;  // both pairs' CTAs
+            const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
+            for (int w = unit; w < nwalk && ok; w += units, ++iter) {
+                const TileInfo t = decode_tile<BN, CG>(P, w * NP + pair);
                 const GemmProblem& pr = P.prob[t.p];
                 const int kblocks = (pr.K + BK - 1) / BK;
                 const int buf = iter & 1;
@@ -379,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     if constexpr (CG == 1)
                         tc_commit<1>(empty0 + 8 * stage);
                     else
-                        tc_commit_pair(empty0 + 8 * stage);
+                        tc_commit_pair(empty0 + 8 * stage, kStageMask);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -389,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 if constexpr (CG == 1)
                     tc_commit<1>(accf0 + 8 * buf);
                 else
-                    tc_commit_pair(accf0 + 8 * buf);
+                    tc_commit_pair(accf0 + 8 * buf, pair_mask);
             }
             // All MMAs issued by this thread must finish before TMEM is freed.
             tc_commit<CG>(drain_bar);
@@ -403,10 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         constexpr int CPW = NCH / 2;            // chunks per warp: two warps share a quarter
         const int cbeg = (ew >> 2) * CPW;       // this warp's first chunk
         const uint32_t stg = smem_u32(sEpi + ew * SBUF);
-        const uint32_t acce_lead = (CG == 2) ? map_to_rank(acce0, 0) : acce0;
+        const uint32_t acce_lead = (CG == 2) ? map_to_rank(acce0, lead) : acce0;
         int iter = 0;
-        for (int tile = unit; tile < P.total_tiles; tile += units, ++iter) {
-            const TileInfo t = decode_tile<BN, CG>(P, tile);
+        for (int w = unit; w < nwalk; w += units, ++iter) {
+            const TileInfo t = decode_tile<BN, CG>(P, w * NP + pair);
             const GemmProblem& pr = P.prob[t.p];
             const int buf = iter & 1;
             const int flags = pr.flags;
@@ -463,41 +493,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const bool diag_block = sym && ((c0 >> 5) == sr);
                 const bool mirror = (flags & kFlagDt) && !diag_block;
 
-                // The staging buffer is free once the previous sub-block's
-                // stores have read it.
-                if (lane == 0) bulk_wait_read<0>();
-                __syncwarp();
-                if (f32) {
-                    stage_row_f32(stg + kOffD, lane, v);
-                } else {
-                    stage_row_f16(stg + kOffD, lane, v);
-                }
-                if (flags & kFlagD2) {
-                    float v2[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v2[j] = pr.delta * v[j] + ((grow == c0 + j) ? pr.gamma : 0.0f);
-                    stage_row_f16(stg + kOffD2, lane, v2);
-                }
-                if (!f32 && (mirror || diag_block)) {
+                // Stage, transpose (mirror or diagonal fix-up) and store one
+                // 32 x 32 block; the buffer is free once the previous stores
+                // have read it.
+                auto emit = [&](const float (&val)[32], int map_d, int map_dt) {
+                    if (lane == 0) bulk_wait_read<0>();
                     __syncwarp();
-                    transpose_block(stg + kOffD, stg + kOffDt, lane);
-                    if (flags & kFlagD2) transpose_block(stg + kOffD2, stg + kOffD2t, lane);
-                    if (diag_block) {
-                        __syncwarp();
-                        merge_upper(stg + kOffD, stg + kOffDt, lane);
-                        if (flags & kFlagD2) merge_upper(stg + kOffD2, stg + kOffD2t, lane);
+                    if (f32) {
+                        stage_row_f32(stg + kOffD, lane, val);
+                    } else {
+                        stage_row_f16(stg + kOffD, lane, val);
+                        if (mirror || diag_block) {
+                            __syncwarp();
+                            transpose_block(stg + kOffD, stg + kOffDt, lane);
+                            if (diag_block) {
+                                __syncwarp();
+                                merge_upper(stg + kOffD, stg + kOffDt, lane);
+                            }
+                        }
                     }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&P.maps[pr.mD], stg + kOffD, c0, r0, t.g);
-                    if (mirror) tma_store_3d(&P.maps[pr.mDt], stg + kOffDt, r0, c0, t.g);
-                    if (flags & kFlagD2) {
-                        tma_store_3d(&P.maps[pr.mD2], stg + kOffD2, c0, r0, t.g);
-                        if (mirror) tma_store_3d(&P.maps[pr.mD2t], stg + kOffD2t, r0, c0, t.g);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&P.maps[map_d], stg + kOffD, c0, r0, t.g);
+                        if (mirror) tma_store_3d(&P.maps[map_dt], stg + kOffDt, r0, c0, t.g);
+                        bulk_commit();
                     }
-                    bulk_commit();
+                };
+                emit(v, pr.mD, pr.mDt);
+                if (flags & kFlagD2) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = pr.delta * v[j] + ((grow == c0 + j) ? pr.gamma : 0.0f);
+                    emit(v, pr.mD2, pr.mD2t);
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) cb[k] = cbn[k];
@@ -525,27 +552,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     tc_fence_before();
     __syncthreads();
-    // The leader's MMAs read the peer's shared memory and the peer's epilogue
-    // arrives on the leader's barriers: neither CTA leaves before both are done.
-    if constexpr (CG == 2) cluster_sync();
+    // The leader's MMAs read the peer's shared memory, multicasts write into
+    // other CTAs and epilogues arrive on the leader's barriers: no CTA of the
+    // cluster leaves before all are done.
+    if constexpr (CL > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, TMEM_COLS);
     }
 }
 
-template <int BN, int CG>
+// Clusters of CL CTAs that can be resident at once with this kernel's
+// shared memory; the grid never exceeds it, so every cluster of a program
+// runs concurrently (tiles wait on tiles of other clusters).
+template <int BN, int CG, int NP>
+int max_clusters(int num_sms) {
+    static int cached = -1;
+    if (cached < 0) {
+        constexpr int CL = CG * NP;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CL * (num_sms / CL));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem_bytes<BN, CG>();
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, CG, NP>, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms / CL;
+        }
+        cached = n;
+    }
+    return cached < num_sms / (CG * NP) ? cached : num_sms / (CG * NP);
+}
+
+template <int BN, int CG, int NP>
 int launch_impl(const GemmProgram& prog, int num_sms, cudaStream_t stream) {
     static bool configured = false;
     constexpr int bytes = smem_bytes<BN, CG>();
+    constexpr int CL = CG * NP;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaError_t e =
+            cudaFuncSetAttribute(gemm_tc_kernel<BN, CG, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     if (prog.total_tiles <= 0) return cudaSuccess;
-    const int units = num_sms / CG;
-    const int grid = CG * (prog.total_tiles < units ? prog.total_tiles : units);
+    if (prog.total_tiles % NP != 0) return cudaErrorInvalidValue;
+    const int walks = prog.total_tiles / NP;
+    const int clusters = max_clusters<BN, CG, NP>(num_sms);
+    const int grid = CL * (walks < clusters ? walks : clusters);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -555,12 +616,12 @@ int launch_impl(const GemmProgram& prog, int num_sms, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = CG;
+    attr[1].val.clusterDim.x = CL;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, CG>, prog);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, CG, NP>, prog);
 }
 
 }  // namespace
@@ -570,22 +631,31 @@ int gemm_smem_bytes(int bn, int cg) {
     return bn == 256 ? smem_bytes<256, 1>() : smem_bytes<128, 1>();
 }
 
-int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym) {
+int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym, int np, bool share, int* walk_n) {
     const int tmh = BM * cg;
     const int tm = (M + tmh - 1) / tmh;
     const int tn = (N + bn - 1) / bn;
-    if (!sym) return tm * tn;
+    const int wn = share ? tn + (tn & 1) : tn;
+    if (walk_n) *walk_n = wn;
     int total = 0;
-    for (int i = 0; i < tm; ++i) total += sym_row_tiles(i, tmh, bn, tn);
+    if (!sym) {
+        total = tm * wn;
+    } else {
+        for (int i = 0; i < tm; ++i) total += sym_row_tiles(i, tmh, bn, tn, share);
+    }
+    if (np == 2) total += total & 1;
     return total;
 }
 
 int gemm_signals_per_tile(int cg) { return kEpiWarps * cg; }
 
-int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream) {
-    if (cg == 2) return launch_impl<256, 2>(prog, num_sms, stream);
-    if (bn == 256) return launch_impl<256, 1>(prog, num_sms, stream);
-    return launch_impl<128, 1>(prog, num_sms, stream);
+int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int np, int num_sms, cudaStream_t stream) {
+    if (cg == 2) {
+        if (np == 2) return launch_impl<256, 2, 2>(prog, num_sms, stream);
+        return launch_impl<256, 2, 1>(prog, num_sms, stream);
+    }
+    if (bn == 256) return launch_impl<256, 1, 1>(prog, num_sms, stream);
+    return launch_impl<128, 1, 1>(prog, num_sms, stream);
 }
 
 }  // namespace gns

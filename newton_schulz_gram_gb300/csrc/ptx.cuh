@@ -158,6 +158,29 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// TMA load written to the same shared-memory offset of every CTA in `mask`
+// (cluster ranks), each completing on its own mbarrier at the same offset.
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
+                                                      int c2, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+        : "memory");
+}
+
+// Multicast TMA load for paired MMAs: written to the same offset of every CTA
+// in `mask`; completion is signalled on the mbarrier at offset `bar` of the
+// pair leader of each destination (bar is given as the leader's address).
+__device__ __forceinline__ void tma_load_3d_multicast_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                                           int c1, int c2, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // TMEM allocation. With CG == 2 one warp of each CTA of the pair executes
@@ -208,11 +231,12 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                      : "memory");
 }
 
-// The same, arriving on the mbarrier at this offset in both CTAs of the pair.
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+// The same, arriving on the mbarrier at this offset in every CTA of `mask`
+// (cluster ranks).
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask = 3) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(static_cast<uint16_t>(3))
+        "h"(mask)
         : "memory");
 }
 
