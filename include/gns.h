@@ -196,9 +196,10 @@ void gns_profile_enable(int on);
 /* Synchronizes the recorded events and returns, per kernel class, the number
  * of profiled launches (counts[k]) and their summed event durations in ms
  * (ms[k]) since the previous read; then forgets them. Classes: 0 tcgen05
- * GEMM, 1 norm (sum of squares), 2 scale/cast/transpose, 3 Muon elementwise,
- * 4 output copy. Writes min(max_classes, 5) entries of each non-null array
- * and returns the number of classes (5), or a negative gns_status. */
+ * GEMM, 1 norm + scale + cast to fp16 (with the momentum update inside
+ * muon_step), 2 Muon elementwise (update / write-back, standalone momentum),
+ * 3 output copy. Writes min(max_classes, 4) entries of each non-null array
+ * and returns the number of classes (4), or a negative gns_status. */
 int gns_profile_read(int64_t* counts, double* ms, int max_classes);
 
 /* Workspace bytes currently held on the current device. */

@@ -176,7 +176,7 @@ def gns_last_error():
     return load().gns_last_error().decode(errors="replace")
 
 
-KERNEL_CLASSES = ("gemm_tc", "sumsq", "scale_cast", "muon_elementwise", "copy_rows")
+KERNEL_CLASSES = ("gemm_tc", "norm_cast", "muon_elementwise", "copy_rows")
 
 
 def gns_launch_count():

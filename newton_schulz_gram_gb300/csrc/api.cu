@@ -126,7 +126,7 @@ int ensure_workspace(DeviceState& st, size_t bytes) {
 // bracketed by a pair of CUDA events on its own stream; gns_profile_read()
 // turns them into per-class launch counts and summed durations.
 
-enum KernelClass { kClsGemm = 0, kClsNorm = 1, kClsCast = 2, kClsMuon = 3, kClsCopy = 4, kNumCls = 5 };
+enum KernelClass { kClsGemm = 0, kClsNorm = 1, kClsMuon = 2, kClsCopy = 3, kNumCls = 4 };
 
 std::atomic<long long> g_launches{0};
 std::atomic<bool> g_profiling{false};
@@ -473,7 +473,7 @@ BucketGeom make_geom(int R, int C) {
 // input's own orientation (R x C): Xa holds X0 (and the standard-NS iterates
 // alternate between Xa and Xb), Xb holds X after the restart.
 struct Layout {
-    size_t xa, xb, r, z, rz, qa, qb, partial, counters, out32, o16, meta, total;
+    size_t xa, xb, r, z, rz, qa, qb, partial, queue, counters, out32, o16, meta, total;
     long long ld_x;
     long long ld_out32;
 };
@@ -496,7 +496,8 @@ Layout make_layout(const BucketGeom& g, int Gc, bool need_out32, bool need_o16, 
     L.rz = g.square ? 0 : take(nn);
     L.qa = g.square ? 0 : take(nn);
     L.qb = g.square ? 0 : take(nn);
-    L.partial = take(static_cast<size_t>(Gc) * 64 * 4);
+    L.partial = take(static_cast<size_t>(Gc) * norm_parts(static_cast<long long>(g.R) * g.C) * 4);
+    L.queue = take((1 + static_cast<size_t>(Gc)) * 4);
     L.counters = take(static_cast<size_t>(Gc) * 4);
     L.ld_out32 = round_up_ll(g.C, 4);
     L.out32 = need_out32 ? take(static_cast<size_t>(g.R) * L.ld_out32 * 4 * Gc) : 0;
@@ -517,18 +518,34 @@ Mat mat16(char* ws, size_t off, int rows, int cols, long long ld) {
     return m;
 }
 
-// Runs the orthogonalization of one chunk of Gc matrices whose sum-of-squares
-// partials are already in L.partial (nblk per matrix).
-int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in, int nblk, int steps,
-             int restart_at, const Coeffs& cf, const OutSpec& os, cudaStream_t s) {
+// Runs the orthogonalization of one chunk of Gc fp32 matrices `in` (the
+// momentum, first updated in place as M <- mu M + G, when grads is given).
+int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in,
+             const MatrixSet* grads, float mu, int steps, int restart_at, const Coeffs& cf, const OutSpec& os,
+             cudaStream_t s) {
     ProgramBuilder prog(st, Gc, choose_tile(g.n), reinterpret_cast<int*>(st.ws + L.counters), s);
     char* ws = st.ws;
     const int n = g.n;
     // Stored copies of X in the input's orientation (R x C).
     Mat Xa = mat16(ws, L.xa, g.R, g.C, L.ld_x);
     Mat Xb = mat16(ws, L.xb, g.R, g.C, L.ld_x);
-    LAUNCH(kClsCast, launch_scale_cast(in, Gc, g.R, g.C, reinterpret_cast<const float*>(ws + L.partial), nblk, g.k_exp,
-                                       Xa.p, Xa.ld, Xa.stride, st.err, s));
+    {
+        NormCastJob job{};
+        job.in = in;
+        if (grads) job.grads = *grads;
+        job.mu = mu;
+        job.G = Gc;
+        job.R = g.R;
+        job.C = g.C;
+        job.k_exp = g.k_exp;
+        job.out = Xa.p;
+        job.ld_out = Xa.ld;
+        job.stride_out = Xa.stride;
+        job.partial = reinterpret_cast<float*>(ws + L.partial);
+        job.queue = reinterpret_cast<int*>(ws + L.queue);
+        job.err = st.err;
+        LAUNCH(kClsNorm, launch_norm_cast(job, st.num_sms, s));
+    }
     const float inv_s = 1.0f / g.s;
     const float out_scale = std::ldexp(1.0f, -g.k_exp);
     // Operand views of the stored X (Xs = X when R <= C, Xs = X^T when R > C):
@@ -740,12 +757,10 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart
     const Layout L = make_layout(g, Gc, !direct_out, false, 0);
     RET(ensure_workspace(*st, L.total));
     const long long numel = static_cast<long long>(R) * C;
-    const int nblk = norm_blocks(numel);
     for (int g0 = 0; g0 < G; g0 += Gc) {
         const int gc = std::min(Gc, G - g0);
         float* base = ptr + static_cast<long long>(g0) * numel;
         MatrixSet in{base, numel, nullptr};
-        LAUNCH(kClsNorm, launch_sumsq(in, numel, gc, reinterpret_cast<float*>(st->ws + L.partial), st->err, s));
         OutSpec os;
         if (direct_out) {
             os.out.p = base;
@@ -762,7 +777,7 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart
             os.out.stride = static_cast<long long>(R) * L.ld_out32;
             os.out.f32 = true;
         }
-        RET(run_core(*st, g, L, gc, in, nblk, steps, restart_at, cf, os, s));
+        RET(run_core(*st, g, L, gc, in, nullptr, 0.0f, steps, restart_at, cf, os, s));
         if (!direct_out)
             LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
     }
@@ -869,8 +884,6 @@ int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tenso
             MatrixSet Ms{nullptr, 0, pm};
             MatrixSet Gs{nullptr, 0, pm + gc};
             MatrixSet Ws{nullptr, 0, pm + 2 * gc};
-            float* partial = reinterpret_cast<float*>(st->ws + L.partial);
-            LAUNCH(kClsMuon, launch_momentum(Ms, Gs, numel, gc, mu, partial, s));
             OutSpec os;
             os.out.p = st->ws + L.o16;
             os.out.rows = R;
@@ -878,7 +891,7 @@ int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tenso
             os.out.ld = ld_o;
             os.out.stride = static_cast<long long>(R) * ld_o;
             os.out.f32 = false;
-            RET(run_core(*st, g, L, gc, Ms, norm_blocks(numel), 5, 2, cf, os, s));
+            RET(run_core(*st, g, L, gc, Ms, &Gs, mu, 5, 2, cf, os, s));
             MatrixSet Os{os.out.p, os.out.stride, nullptr};
             LAUNCH(kClsMuon, launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s));
         }
@@ -894,7 +907,7 @@ int gns_muon_momentum(float* M, const uint16_t* G_bf16, int64_t numel, float mu,
     MatrixSet Ms{M, numel, nullptr};
     MatrixSet Gs{G_bf16, numel, nullptr};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    LAUNCH(kClsMuon, launch_momentum(Ms, Gs, numel, 1, mu, nullptr, s));
+    LAUNCH(kClsMuon, launch_momentum(Ms, Gs, numel, 1, mu, s));
     return GNS_OK;
 }
 
@@ -1122,12 +1135,10 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
     CK(cudaMemsetAsync(st.err, 0, sizeof(int), s));
 
     const long long numel = static_cast<long long>(R) * C;
-    const int nblk = norm_blocks(numel);
     for (int g0 = 0; g0 < G; g0 += Gc) {
         const int gc = std::min(Gc, G - g0);
         float* base = ptr + static_cast<long long>(g0) * numel;
         MatrixSet in{base, numel, nullptr};
-        LAUNCH(kClsNorm, launch_sumsq(in, numel, gc, reinterpret_cast<float*>(st.ws + L.partial), st.err, s));
         OutSpec os;
         os.out.rows = R;
         os.out.cols = C;
@@ -1141,7 +1152,7 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
             os.out.ld = L.ld_out32;
             os.out.stride = static_cast<long long>(R) * L.ld_out32;
         }
-        RET(run_core(st, g, L, gc, in, nblk, steps, restart_at, cf, os, s));
+        RET(run_core(st, g, L, gc, in, nullptr, 0.0f, steps, restart_at, cf, os, s));
         if (!direct_out)
             LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
     }

@@ -16,6 +16,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <cstdlib>
+
 #include "elementwise.cuh"
 #include "ptx.cuh"
 
@@ -57,106 +60,366 @@ __device__ __forceinline__ long long chunk_len(long long numel, int nblk) {
     return (((numel + nblk - 1) / nblk) + 3) & ~3LL;
 }
 
-// Fixed-order block reduction of one float per thread.
-__device__ __forceinline__ float block_sum(float v) {
-    __shared__ float red[kThreads / 32];
+// M <- mu M + G over [beg, end) (beg a multiple of 4), fp32 with two
+// roundings, by a worker of NT threads (t its thread index); returns the sum of
+// squares of this thread's new M values.
+template <int NT>
+__device__ __forceinline__ float momentum_range(float* M, const __nv_bfloat16* Gr, long long beg, long long end,
+                                                float mu, int t) {
+    constexpr long long kStep = 4LL * NT;
+    float s = 0.0f;
+    long long i = beg + 4LL * t;
+    auto upd = [&](float4& m, uint2 graw) {
+        const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&graw);
+        const float2 g01 = __bfloat1622float2(gb[0]);
+        const float2 g23 = __bfloat1622float2(gb[1]);
+        m.x = __fadd_rn(__fmul_rn(mu, m.x), g01.x);
+        m.y = __fadd_rn(__fmul_rn(mu, m.y), g01.y);
+        m.z = __fadd_rn(__fmul_rn(mu, m.z), g23.x);
+        m.w = __fadd_rn(__fmul_rn(mu, m.w), g23.y);
+        s = fmaf(m.x, m.x, s);
+        s = fmaf(m.y, m.y, s);
+        s = fmaf(m.z, m.z, s);
+        s = fmaf(m.w, m.w, s);
+    };
+    const bool vec = ((reinterpret_cast<uintptr_t>(M) & 15) == 0) && ((reinterpret_cast<uintptr_t>(Gr) & 7) == 0);
+    if (vec) {
+        for (; i + 3 * kStep + 3 < end; i += 4 * kStep) {
+            float4 m[4];
+            uint2 gr[4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float t = 0.0f;
-    if (threadIdx.x == 0) {
-        for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+            for (int u = 0; u < 4; ++u) {
+                m[u] = __ldcg(reinterpret_cast<const float4*>(M + i + u * kStep));
+                gr[u] = __ldcg(reinterpret_cast<const uint2*>(Gr + i + u * kStep));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                upd(m[u], gr[u]);
+                *reinterpret_cast<float4*>(M + i + u * kStep) = m[u];
+            }
+        }
+        for (; i + 3 < end; i += kStep) {
+            float4 m = __ldcg(reinterpret_cast<const float4*>(M + i));
+            upd(m, __ldcg(reinterpret_cast<const uint2*>(Gr + i)));
+            *reinterpret_cast<float4*>(M + i) = m;
+        }
     }
-    __syncthreads();
-    return t;  // valid in thread 0
+    for (; i < end; i += kStep) {
+        for (int e = 0; e < 4; ++e) {
+            if (i + e < end) {
+                const float m = __fadd_rn(__fmul_rn(mu, M[i + e]), __bfloat162float(Gr[i + e]));
+                M[i + e] = m;
+                s = fmaf(m, m, s);
+            }
+        }
+    }
+    return s;
 }
 
-// Sum of x^2 over [beg, end) of x, each thread over a fixed stride.
-__device__ __forceinline__ float chunk_sumsq(const float* x, long long beg, long long end) {
+// ---------------------------------------------------- norm + cast items
+//
+// An item is elements [beg, end) of one matrix, flattened row-major; a full
+// item has kNormPartElems = 4 kItemVec kThreads elements (64 KB of fp32), and
+// thread t owns its groups of 4 at beg + 4 (t + kThreads u), u = 0 ..
+// kItemVec - 1. All kItemVec loads of a thread are issued before the first
+// is used.
+constexpr int kItemVec = 16;
+static_assert(kNormPartElems == 4LL * kThreads * kItemVec, "a full norm part is one item");
+
+__device__ __forceinline__ bool item_full(const void* x, long long beg, long long end) {
+    return end - beg == kNormPartElems && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+}
+
+// The kItemVec float4 of a full item owned by this thread.
+struct ItemRegs {
+    float4 f[kItemVec];
+};
+
+__device__ __forceinline__ void item_load(ItemRegs& r, const float* x, long long beg, long long end) {
+    if (item_full(x, beg, end)) {
+        const float4* v = reinterpret_cast<const float4*>(x + beg) + threadIdx.x;
+#pragma unroll
+        for (int u = 0; u < kItemVec; ++u) r.f[u] = __ldcg(v + kThreads * u);
+    }
+}
+
+// This thread's sum of squares over its groups of the item, u ascending
+// (from the registers item_load filled, for a full item).
+__device__ __forceinline__ float item_sumsq(const ItemRegs& r, const float* x, long long beg, long long end) {
     float s = 0.0f;
-    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    long long i = beg + 4LL * threadIdx.x;
-    if (vec) {
-        for (; i + 3 < end; i += 4LL * kThreads) {
-            const float4 f = *reinterpret_cast<const float4*>(x + i);
-            s = fmaf(f.x, f.x, s);
-            s = fmaf(f.y, f.y, s);
-            s = fmaf(f.z, f.z, s);
-            s = fmaf(f.w, f.w, s);
+    if (item_full(x, beg, end)) {
+#pragma unroll
+        for (int u = 0; u < kItemVec; ++u) {
+            s = fmaf(r.f[u].x, r.f[u].x, s);
+            s = fmaf(r.f[u].y, r.f[u].y, s);
+            s = fmaf(r.f[u].z, r.f[u].z, s);
+            s = fmaf(r.f[u].w, r.f[u].w, s);
         }
-        for (int e = 0; e < 4; ++e)
-            if (i + e < end) s = fmaf(x[i + e], x[i + e], s);
     } else {
-        for (; i < end; i += 4LL * kThreads)
+        for (long long i = beg + 4LL * threadIdx.x; i < end; i += 4LL * kThreads)
             for (int e = 0; e < 4; ++e)
                 if (i + e < end) s = fmaf(x[i + e], x[i + e], s);
     }
     return s;
 }
 
-__global__ void __launch_bounds__(kThreads) sumsq_kernel(MatrixSet in, long long numel, int nblk,
-                                                         float* partial) {
-    grid_dependency_wait();
-    grid_launch_dependents();
-    const float* x = mat_f32(in, blockIdx.y);
-    const long long chunk = chunk_len(numel, nblk);
-    const long long beg = static_cast<long long>(blockIdx.x) * chunk;
-    const long long end = beg + chunk < numel ? beg + chunk : numel;
-    const float t = block_sum(beg < end ? chunk_sumsq(x, beg, end) : 0.0f);
-    if (threadIdx.x == 0) partial[static_cast<long long>(blockIdx.y) * nblk + blockIdx.x] = t;
+__device__ __forceinline__ float4 momentum4(float4 m, uint2 graw, float mu) {
+    const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&graw);
+    const float2 g01 = __bfloat1622float2(gb[0]);
+    const float2 g23 = __bfloat1622float2(gb[1]);
+    m.x = __fadd_rn(__fmul_rn(mu, m.x), g01.x);
+    m.y = __fadd_rn(__fmul_rn(mu, m.y), g01.y);
+    m.z = __fadd_rn(__fmul_rn(mu, m.z), g23.x);
+    m.w = __fadd_rn(__fmul_rn(mu, m.w), g23.y);
+    return m;
 }
 
-// Scale and cast, in the input's own layout: 4 consecutive elements per
-// thread (vector load and store when aligned), grid-stride over the matrix.
-__global__ void __launch_bounds__(kThreads) scale_cast_kernel(MatrixSet in, int R, int C, const float* partial,
-                                                              int nblk, int k_exp, __half* out, long long ld_o,
-                                                              long long stride_o, int* err) {
-    __shared__ float s_scale;
-    grid_dependency_wait();
-    grid_launch_dependents();
-    const int g = blockIdx.y;
-    if (threadIdx.x == 0) {
-        float t = 0.0f;
-        const float* p = partial + static_cast<long long>(g) * nblk;
-        for (int b = 0; b < nblk; ++b) t += p[b];
-        const float norm = sqrtf(t);
-        if (!isfinite(norm)) raise_error(err, kDevErrNonFinite);
-        s_scale = ldexpf(1.0f, k_exp) / (1.05f * (norm + 1e-7f));
-    }
-    __syncthreads();
-    const float scale = s_scale;
-    const float* x = mat_f32(in, g);
-    __half* og = out + static_cast<long long>(g) * stride_o;
-    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && (C % 4 == 0);
-    const long long groups_per_row = (C + 3) / 4;
-    const long long groups = static_cast<long long>(R) * groups_per_row;
-    for (long long q = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; q < groups;
-         q += static_cast<long long>(gridDim.x) * kThreads) {
-        const long long r = q / groups_per_row;
-        const int c = static_cast<int>(q - r * groups_per_row) * 4;
-        const float* src = x + r * C + c;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (vec) {
-            const float4 f = *reinterpret_cast<const float4*>(src);
-            v[0] = f.x;
-            v[1] = f.y;
-            v[2] = f.z;
-            v[3] = f.w;
-        } else {
-            for (int e = 0; e < 4; ++e)
-                if (c + e < C) v[e] = src[e];
+// M <- mu M + G over the item; returns this thread's sum of squares of the
+// new M (same element order as item_sumsq).
+__device__ __forceinline__ float item_momentum(float* M, const __nv_bfloat16* Gr, long long beg, long long end,
+                                               float mu) {
+    float s = 0.0f;
+    if (item_full(M, beg, end) && (reinterpret_cast<uintptr_t>(Gr) & 7) == 0) {
+        float4* mv = reinterpret_cast<float4*>(M + beg) + threadIdx.x;
+        const uint2* gv = reinterpret_cast<const uint2*>(Gr + beg) + threadIdx.x;
+#pragma unroll
+        for (int h = 0; h < kItemVec; h += kItemVec / 2) {
+            float4 m[kItemVec / 2];
+            uint2 gr[kItemVec / 2];
+#pragma unroll
+            for (int u = 0; u < kItemVec / 2; ++u) {
+                m[u] = __ldcg(mv + kThreads * (h + u));
+                gr[u] = __ldcg(gv + kThreads * (h + u));
+            }
+#pragma unroll
+            for (int u = 0; u < kItemVec / 2; ++u) {
+                const float4 n = momentum4(m[u], gr[u], mu);
+                mv[kThreads * (h + u)] = n;
+                s = fmaf(n.x, n.x, s);
+                s = fmaf(n.y, n.y, s);
+                s = fmaf(n.z, n.z, s);
+                s = fmaf(n.w, n.w, s);
+            }
         }
-        __half* dst = og + r * ld_o + c;
-        // ld_o is a multiple of 8 halves and c of 4: 8-byte aligned; columns
-        // past C land in the row padding.
-        __half2 h01 = __floats2half2_rn(v[0] * scale, v[1] * scale);
-        __half2 h23 = __floats2half2_rn(v[2] * scale, v[3] * scale);
+    } else {
+        for (long long i = beg + 4LL * threadIdx.x; i < end; i += 4LL * kThreads) {
+            for (int e = 0; e < 4; ++e) {
+                if (i + e < end) {
+                    const float m = __fadd_rn(__fmul_rn(mu, M[i + e]), __bfloat162float(Gr[i + e]));
+                    M[i + e] = m;
+                    s = fmaf(m, m, s);
+                }
+            }
+        }
+    }
+    return s;
+}
+
+// The cast of one item: out = fp16(scale x); element i of the matrix goes
+// to row i / C, column i % C of out (row stride ld_o, a multiple of 8
+// halves). A full item with C % 4 == 0 casts the registers item_load filled.
+__device__ __forceinline__ bool cast_fast(const float* x, long long beg, long long end, int C) {
+    return item_full(x, beg, end) && C % 4 == 0;
+}
+
+__device__ __forceinline__ void item_cast_store(const ItemRegs& r, const float* x, long long beg, long long end, int C,
+                                                float scale, __half* out, long long ld_o) {
+    auto h4 = [&](float4 f) {
+        __half2 h01 = __floats2half2_rn(f.x * scale, f.y * scale);
+        __half2 h23 = __floats2half2_rn(f.z * scale, f.w * scale);
         uint2 packed;
         packed.x = *reinterpret_cast<uint32_t*>(&h01);
         packed.y = *reinterpret_cast<uint32_t*>(&h23);
-        *reinterpret_cast<uint2*>(dst) = packed;
+        return packed;
+    };
+    if (cast_fast(x, beg, end, C)) {
+        if (ld_o == C) {
+            uint2* o = reinterpret_cast<uint2*>(out + beg) + threadIdx.x;
+#pragma unroll
+            for (int u = 0; u < kItemVec; ++u) o[kThreads * u] = h4(r.f[u]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < kItemVec; ++u) {
+                const long long i = beg + 4LL * (threadIdx.x + kThreads * u);
+                const long long row = i / C;
+                *reinterpret_cast<uint2*>(out + row * ld_o + (i - row * C)) = h4(r.f[u]);
+            }
+        }
+    } else {
+        for (long long i = beg + threadIdx.x; i < end; i += kThreads) {
+            const long long row = i / C;
+            out[row * ld_o + (i - row * C)] = __float2half_rn(x[i] * scale);
+        }
     }
+}
+
+// ------------------------------------------------------ norm + cast queue
+//
+// One pass over the bucket. Matrices are taken in chunks of `mpc`; the work
+// items are the norm parts S_c of chunk c (sum of squares, optionally after
+// the momentum update) and its cast items C_c (the same element ranges).
+// Blocks draw items from a ticket counter in the order S_0 .. S_{L-1}, then
+// S_{c+L}, C_c for c = 0, 1, ...: a chunk is cast L chunks after it was
+// summed, while it is still in L2. A norm part stores its partial sum and
+// counts itself done (release, no wait). A cast item issues its loads, waits
+// until every part of its matrix is done, sums the partials in a fixed order
+// (the same in every cast item, so every item gets the same scale) and
+// stores. A block holds at most two tickets (the item it works on and the
+// next one) and works through them in order; every part a cast item waits
+// for has a smaller ticket, held by a running block, so by induction on the
+// ticket every wait ends, whatever the grid size and residency.
+struct NormCastArgs {
+    NormCastJob j;
+    long long numel, part_len;
+    int nparts, mpc, nchunks, lag, total;
+};
+
+struct NcItem {
+    int sum;  // 1 norm part, 0 cast item
+    int g, part;
+};
+
+// Round r of the queue is S_r (if r < nchunks) followed by C_{r-L} (if
+// r >= L). Chunks hold mpc matrices except possibly the last, so the first
+// k chunks hold min(k mpc, G) matrices, and round r starts at ticket
+// nparts (mats(min(r, n)) + mats(clamp(r - L, 0, n))).
+__device__ __forceinline__ int nc_mats_before(const NormCastArgs& a, int k) {
+    const long long m = static_cast<long long>(k) * a.mpc;
+    return m < a.j.G ? static_cast<int>(m) : a.j.G;
+}
+
+__device__ __forceinline__ long long nc_round_start(const NormCastArgs& a, int r) {
+    const int rs = r < a.nchunks ? r : a.nchunks;
+    int rc = r - a.lag;
+    rc = rc < 0 ? 0 : (rc > a.nchunks ? a.nchunks : rc);
+    return static_cast<long long>(a.nparts) * (nc_mats_before(a, rs) + nc_mats_before(a, rc));
+}
+
+__device__ NcItem nc_decode(const NormCastArgs& a, int q) {
+    // Largest round r with start(r) <= q (start is non-decreasing in r).
+    int lo = 0, hi = a.nchunks + a.lag;  // start(hi) = total > q
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (nc_round_start(a, mid) <= q)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int r = lo;
+    int o = static_cast<int>(q - nc_round_start(a, r));
+    if (r < a.nchunks) {
+        const int ssize = (nc_mats_before(a, r + 1) - nc_mats_before(a, r)) * a.nparts;
+        if (o < ssize) return {1, r * a.mpc + o / a.nparts, o % a.nparts};
+        o -= ssize;
+    }
+    const int c = r - a.lag;
+    return {0, c * a.mpc + o / a.nparts, o % a.nparts};
+}
+
+template <bool kMomentum>
+__global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_constant__ NormCastArgs a) {
+    __shared__ float red[kThreads / 32];
+    __shared__ int s_next;
+    __shared__ float s_scale;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    int* ticket = a.j.queue;
+    int* ready = a.j.queue + 1;
+    // Thread 0 releases a finished part's count at the start of its block's
+    // next item, after that item's loads are issued, so the release latency
+    // overlaps them; always before any wait of that item.
+    int pending = -1;
+    auto release_pending = [&]() {
+        if (t == 0 && pending >= 0) {
+            red_release_add(ready + pending, 1);
+            pending = -1;
+        }
+    };
+    if (t == 0) s_next = atomicAdd(ticket, 1);
+    __syncthreads();
+    int q = s_next;
+    while (q < a.total) {
+        __syncthreads();  // every thread has read s_next
+        // The next ticket is taken now; its value is needed only at the end.
+        int nxt = 0;
+        if (t == 0) nxt = atomicAdd(ticket, 1);
+        const NcItem it = nc_decode(a, q);
+        const long long beg = it.part * a.part_len;
+        const long long end = beg + a.part_len < a.numel ? beg + a.part_len : a.numel;
+        ItemRegs regs;
+        if (it.sum) {
+            float s;
+            if constexpr (kMomentum) {
+                release_pending();
+                s = item_momentum(mat_ptr<float>(a.j.in, it.g), mat_ptr<const __nv_bfloat16>(a.j.grads, it.g), beg,
+                                  end, a.j.mu);
+            } else {
+                const float* x = mat_f32(a.j.in, it.g);
+                item_load(regs, x, beg, end);
+                release_pending();
+                s = item_sumsq(regs, x, beg, end);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) red[warp] = s;
+            // The barrier also orders every thread's M stores (momentum) before
+            // thread 0's release.
+            __syncthreads();
+            if (t == 0) {
+                float v = 0.0f;
+                for (int w = 0; w < kThreads / 32; ++w) v += red[w];
+                a.j.partial[static_cast<long long>(it.g) * a.nparts + it.part] = v;
+                pending = it.g;
+            }
+        } else {
+            const float* x = mat_f32(a.j.in, it.g);
+            // The input is read-only here, so its loads may start before the
+            // wait; the momentum is written by this kernel and is read after.
+            if constexpr (!kMomentum) item_load(regs, x, beg, end);
+            release_pending();
+            if (warp == 0) {
+                // Every part of matrix g summed: fixed-order sum of its partials
+                // (the same in every cast item of g).
+                bool ok = true;
+                if (lane == 0) ok = wait_counter(ready + it.g, a.nparts, a.j.err);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (ok) (void)ld_acquire(ready + it.g);
+                // Lane l adds partials l, l + 32, l + 64, ... in that order; the
+                // loads of 8 of them are issued together.
+                const float* p = a.j.partial + static_cast<long long>(it.g) * a.nparts;
+                float v = 0.0f;
+                if (ok) {
+                    for (int b0 = 0; b0 < a.nparts; b0 += 32 * 8) {
+                        float pv[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int b = b0 + lane + 32 * u;
+                            pv[u] = b < a.nparts ? __ldcg(p + b) : 0.0f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) v += pv[u];
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) {
+                    const float norm = sqrtf(v);
+                    if (ok && !isfinite(norm)) raise_error(a.j.err, kDevErrNonFinite);
+                    s_scale = ok ? ldexpf(1.0f, a.j.k_exp) / (1.05f * (norm + 1e-7f)) : 0.0f;
+                }
+            }
+            __syncthreads();
+            if constexpr (kMomentum) item_load(regs, x, beg, end);
+            item_cast_store(regs, x, beg, end, a.j.C, s_scale,
+                            static_cast<__half*>(a.j.out) + static_cast<long long>(it.g) * a.j.stride_out,
+                            a.j.ld_out);
+        }
+        if (t == 0) s_next = nxt;
+        __syncthreads();
+        q = s_next;
+    }
+    release_pending();
 }
 
 __global__ void __launch_bounds__(kThreads) copy_rows_kernel(const float* in, long long ld_in, long long stride_in,
@@ -172,50 +435,18 @@ __global__ void __launch_bounds__(kThreads) copy_rows_kernel(const float* in, lo
     }
 }
 
+// Momentum alone (no norm): blocks over fixed chunks of each matrix.
 __global__ void __launch_bounds__(kThreads) momentum_kernel(MatrixSet Ms, MatrixSet Gs, long long numel, int nblk,
-                                                            float mu, float* partial) {
+                                                            float mu) {
     grid_dependency_wait();
     grid_launch_dependents();
     const int g = blockIdx.y;
-    float* M = mat_ptr<float>(Ms, g);
-    const __nv_bfloat16* Gr = mat_ptr<const __nv_bfloat16>(Gs, g);
     const long long chunk = chunk_len(numel, nblk);
     const long long beg = static_cast<long long>(blockIdx.x) * chunk;
     const long long end = beg + chunk < numel ? beg + chunk : numel;
-    float s = 0.0f;
-    const bool vec = ((reinterpret_cast<uintptr_t>(M) & 15) == 0) && ((reinterpret_cast<uintptr_t>(Gr) & 7) == 0);
-    long long i = beg + 4LL * threadIdx.x;
-    if (vec) {
-        for (; i + 3 < end; i += 4LL * kThreads) {
-            float4 m = *reinterpret_cast<const float4*>(M + i);
-            const uint2 graw = *reinterpret_cast<const uint2*>(Gr + i);
-            const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&graw);
-            const float2 g01 = __bfloat1622float2(gb[0]);
-            const float2 g23 = __bfloat1622float2(gb[1]);
-            m.x = __fadd_rn(__fmul_rn(mu, m.x), g01.x);
-            m.y = __fadd_rn(__fmul_rn(mu, m.y), g01.y);
-            m.z = __fadd_rn(__fmul_rn(mu, m.z), g23.x);
-            m.w = __fadd_rn(__fmul_rn(mu, m.w), g23.y);
-            *reinterpret_cast<float4*>(M + i) = m;
-            s = fmaf(m.x, m.x, s);
-            s = fmaf(m.y, m.y, s);
-            s = fmaf(m.z, m.z, s);
-            s = fmaf(m.w, m.w, s);
-        }
-    }
-    for (; i < end; i += 4LL * kThreads) {
-        for (int e = 0; e < 4; ++e) {
-            if (i + e < end) {
-                const float m = __fadd_rn(__fmul_rn(mu, M[i + e]), __bfloat162float(Gr[i + e]));
-                M[i + e] = m;
-                s = fmaf(m, m, s);
-            }
-        }
-    }
-    if (partial) {
-        const float t = block_sum(s);
-        if (threadIdx.x == 0) partial[static_cast<long long>(g) * nblk + blockIdx.x] = t;
-    }
+    if (beg < end)
+        momentum_range<kThreads>(mat_ptr<float>(Ms, g), mat_ptr<const __nv_bfloat16>(Gs, g), beg, end, mu,
+                                 threadIdx.x);
 }
 
 __device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
@@ -314,26 +545,50 @@ int grid_for(long long work, int per_block_items) {
 
 }  // namespace
 
-int norm_blocks(long long numel) {
-    long long b = numel / (1 << 16);
-    if (b < 1) b = 1;
-    if (b > 64) b = 64;
-    return static_cast<int>(b);
-}
-
-int launch_sumsq(const MatrixSet& in, long long numel, int G, float* partial, int* err, cudaStream_t s) {
-    (void)err;
-    if (G <= 0 || numel <= 0) return cudaSuccess;
-    const int nblk = norm_blocks(numel);
-    return launch_pdl(sumsq_kernel, dim3(nblk, G), dim3(kThreads), s, in, numel, nblk, partial);
-}
-
-int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* partial, int nblk, int k_exp, void* out,
-                      long long ld_out, long long stride_out, int* err, cudaStream_t s) {
-    if (G <= 0) return cudaSuccess;
-    const long long groups = static_cast<long long>(R) * ((C + 3) / 4);
-    return launch_pdl(scale_cast_kernel, dim3(grid_for(groups, kThreads * 8), G), dim3(kThreads), s, in, R, C, partial,
-                      nblk, k_exp, static_cast<__half*>(out), ld_out, stride_out, err);
+int launch_norm_cast(const NormCastJob& job, int num_sms, cudaStream_t s) {
+    if (job.G <= 0) return cudaSuccess;
+    NormCastArgs a{};
+    a.j = job;
+    a.numel = static_cast<long long>(job.R) * job.C;
+    a.nparts = norm_parts(a.numel);
+    a.part_len = norm_part_len(a.numel);
+    const bool momentum = job.grads.base || job.grads.ptrs;
+    // Between its sum and its cast a chunk stays in L2 while the next chunk
+    // is summed and the items in flight (two per block, 64 KB each) complete, so
+    // both the chunk and the number of blocks are kept small. GNS_NC_CHUNK_MB
+    // and GNS_NC_BLOCKS_PER_SM override them (tuning).
+    long long chunk_bytes = 16LL << 20;
+    if (const char* e = std::getenv("GNS_NC_CHUNK_MB")) {
+        if (std::atoll(e) > 0) chunk_bytes = std::atoll(e) << 20;
+    }
+    a.lag = 1;
+    if (const char* e = std::getenv("GNS_NC_LAG")) {
+        if (std::atoi(e) > 0) a.lag = std::atoi(e);
+    }
+    int blocks_per_sm = 2;
+    if (const char* e = std::getenv("GNS_NC_BLOCKS_PER_SM")) {
+        if (std::atoi(e) > 0) blocks_per_sm = std::atoi(e);
+    }
+    const long long per = a.numel * (momentum ? 6 : 4);
+    a.mpc = static_cast<int>(std::max(1LL, std::min<long long>(job.G, chunk_bytes / std::max(per, 1LL))));
+    a.nchunks = (job.G + a.mpc - 1) / a.mpc;
+    const long long total = static_cast<long long>(job.G) * 2 * a.nparts;
+    if (total > (1LL << 30)) return cudaErrorInvalidValue;
+    a.total = static_cast<int>(total);
+    cudaError_t e = cudaMemsetAsync(job.queue, 0, sizeof(int) * (1 + static_cast<size_t>(job.G)), s);
+    if (e != cudaSuccess) return e;
+    static int per_sm[2] = {0, 0};
+    int& occ = per_sm[momentum ? 1 : 0];
+    if (occ == 0) {
+        e = momentum ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, norm_cast_kernel<true>, kThreads, 0)
+                     : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, norm_cast_kernel<false>, kThreads, 0);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) occ = 1;
+    }
+    const long long grid = std::min<long long>(static_cast<long long>(num_sms) * std::min(occ, blocks_per_sm), a.total);
+    if (momentum)
+        return launch_pdl(norm_cast_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), s, a);
+    return launch_pdl(norm_cast_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), s, a);
 }
 
 int launch_copy_rows_f32(const float* in, long long ld_in, long long stride_in, float* out, int G, int R, int C,
@@ -344,11 +599,10 @@ int launch_copy_rows_f32(const float* in, long long ld_in, long long stride_in, 
                       stride_in, out, R, C);
 }
 
-int launch_momentum(const MatrixSet& M, const MatrixSet& Gr, long long numel, int count, float mu, float* partial,
-                    cudaStream_t s) {
+int launch_momentum(const MatrixSet& M, const MatrixSet& Gr, long long numel, int count, float mu, cudaStream_t s) {
     if (count <= 0 || numel <= 0) return cudaSuccess;
-    const int nblk = partial ? norm_blocks(numel) : grid_for(numel, kThreads * 16);
-    return launch_pdl(momentum_kernel, dim3(nblk, count), dim3(kThreads), s, M, Gr, numel, nblk, mu, partial);
+    const int nblk = grid_for(numel, kThreads * 16);
+    return launch_pdl(momentum_kernel, dim3(nblk, count), dim3(kThreads), s, M, Gr, numel, nblk, mu);
 }
 
 int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o, const long long* base_dev,

@@ -14,29 +14,53 @@ struct MatrixSet {
     const void* const* ptrs;
 };
 
-// Number of partial sums per matrix for the deterministic norm (depends on
-// the matrix size only, so results never depend on the bucket size G).
-int norm_blocks(long long numel);
+// The Frobenius norm is summed in parts of norm_part_len(numel) elements
+// (the last one shorter), norm_parts(numel) per matrix: a function of the
+// matrix size only, so a matrix's scale never depends on its bucket.
+constexpr long long kNormPartElems = 16384;
+constexpr int kMaxNormParts = 8192;
 
-// partial[g * nblk + b] = sum of squares of chunk b of fp32 matrix g.
-int launch_sumsq(const MatrixSet& in, long long numel, int G, float* partial, int* err,
-                 cudaStream_t s);
+__host__ __device__ inline long long norm_part_len(long long numel) {
+    const long long even = (numel + kMaxNormParts - 1) / kMaxNormParts;
+    const long long len = (even + 3) & ~3LL;
+    return len > kNormPartElems ? len : kNormPartElems;
+}
 
-// Scale and cast an fp32 R x C matrix set to fp16 in the same layout:
-//   scale_g = 2^k / (1.05 * (sqrt(sum_b partial[g][b]) + 1e-7)),
-//   out[g] (R x C, row stride ld_out, a multiple of 8) = fp16(scale_g * x).
-// A non-finite norm raises the non-finite error word.
-int launch_scale_cast(const MatrixSet& in, int G, int R, int C, const float* partial, int nblk, int k_exp, void* out,
-                      long long ld_out, long long stride_out, int* err, cudaStream_t s);
+__host__ __device__ inline int norm_parts(long long numel) {
+    const long long len = norm_part_len(numel);
+    const long long p = (numel + len - 1) / len;
+    return static_cast<int>(p < 1 ? 1 : p);
+}
+
+// Norm, scale and cast of a bucket of G fp32 R x C matrices in one pass:
+//   [momentum only] M[g] <- mu M[g] + float(grads[g]) (in place, fp32),
+//   scale_g = 2^k_exp / (1.05 (||x_g||_F + 1e-7)),
+//   out[g] (R x C, row stride ld_out, a multiple of 8) = fp16(scale_g x_g).
+// partial holds G * norm_parts(R C) floats and queue 1 + G ints (zeroed
+// here, stream-ordered). A non-finite norm raises the
+// non-finite error word.
+struct NormCastJob {
+    MatrixSet in;     // fp32 input matrices, or the momentum M (updated in place)
+    MatrixSet grads;  // bf16 gradients; base and ptrs both null: no momentum update
+    float mu;
+    int G, R, C;
+    int k_exp;
+    void* out;
+    long long ld_out, stride_out;
+    float* partial;
+    int* queue;
+    int* err;
+};
+
+int launch_norm_cast(const NormCastJob& job, int num_sms, cudaStream_t s);
 
 // out[g] (R x C, contiguous) = in[g] (R x C, row stride ld_in), fp32.
 int launch_copy_rows_f32(const float* in, long long ld_in, long long stride_in, float* out, int G,
                          int R, int C, cudaStream_t s);
 
-// M[g] <- mu * M[g] + float(G[g]); optionally per-matrix sum-of-squares
-// partials of the new M (same chunking as launch_sumsq).
+// M[g] <- mu * M[g] + float(G[g]), fp32 with two roundings.
 int launch_momentum(const MatrixSet& M, const MatrixSet& Gr, long long numel, int count, float mu,
-                    float* partial, cudaStream_t s);
+                    cudaStream_t s);
 
 // W[g] <- SR_bf16((1 - lr wd) W[g] - (lr scale) O[g]) with Philox keyed by
 // (seed, step, base + i), base = base_dev[g] when base_dev is not null, else

@@ -33,7 +33,7 @@ enum GemmFlags : int {
                       // and share (multicast) their A operand
 };
 
-constexpr int kMaxMaps = 24;
+constexpr int kMaxMaps = 64;
 constexpr int kMaxProblems = 48;
 constexpr int kMaxPhases = 40;
 
