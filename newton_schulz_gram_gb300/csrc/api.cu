@@ -232,10 +232,14 @@ struct ProblemSpec {
     float alpha = 1.f, beta = 0.f, delta = 0.f, gamma = 0.f;
     bool sym = false;
     bool reverse = false;  // visit matrices last to first (starts on L2-resident data)
+    // Lower-only storage of symmetric matrices (square tile shapes only):
+    // A / B are read that way, D (and D2) are written that way.
+    bool a_sym = false, b_sym = false, lower = false;
 };
 
-// Tile shape for a program: 256 x 256 tiles on CTA pairs, two pairs per
-// cluster, when the matrices fill them; else 128 x 128 tiles on single CTAs.
+// Tile shape for a program: 256 x 256 tiles on CTA pairs (two pairs per
+// cluster for n >= 3072) when the matrices fill them; else 128 x 128 tiles on
+// single CTAs.
 // GNS_TILE=128x1|256x1|256x2|256x2x2 forces one shape (tuning). With two
 // pairs per cluster, non-symmetric products share their A operand between
 // the pairs (multicast); symmetric ones only when GNS_SHARE_SYM=1 (their
@@ -253,7 +257,10 @@ TileShape choose_tile(int n) {
         if (f == "256x2") return {256, 2, 1};
         if (f == "256x2x2") return {256, 2, 2};
     }
-    return n >= 192 ? TileShape{256, 2, 2} : TileShape{128, 1, 1};
+    if (n < 192) return {128, 1, 1};
+    // Two pairs per cluster (A shared) pay off only for large matrices: the
+    // 4-CTA clusters leave 8 of the 152 SMs idle.
+    return n >= 3072 ? TileShape{256, 2, 2} : TileShape{256, 2, 1};
 }
 
 bool share_symmetric() {
@@ -359,7 +366,10 @@ class ProgramBuilder {
         if (sp.D2 && sp.Dt && !sp.D2t) return fail(GNS_ERR_INVALID, "second output needs its transposed map");
         if (sp.D.f32 && (sp.Dt || sp.D2)) return fail(GNS_ERR_INVALID, "fp32 output supports no transposed/second output");
         if (G_ > 65535) return fail(GNS_ERR_INVALID, "too many matrices in one launch");
-        pr.mA = pr.mB = pr.mD = pr.mDt = pr.mD2 = pr.mD2t = -1;
+        pr.mA = pr.mB = pr.mD = pr.mDt = pr.mD2 = pr.mD2t = pr.mAt = pr.mBt = -1;
+        if ((sp.a_sym || sp.b_sym || sp.lower) && bn != 128 * cg)
+            return fail(GNS_ERR_INVALID, "lower-only storage needs square tiles");
+        if ((sp.a_sym && sp.a_mn) || (sp.b_sym && sp.b_mn)) return fail(GNS_ERR_INVALID, "lower-only operands are K-major");
         RET(operand(sp.A, sp.a_mn ? 64u : 128u, pr.mA, sp.a_mn));
         RET(operand(sp.B, sp.b_mn ? 64u : static_cast<uint32_t>(bn / cg), pr.mB, sp.b_mn));
         RET(output(sp.D, pr.mD));
@@ -368,6 +378,15 @@ class ProgramBuilder {
         if (sp.D.f32) flags |= kFlagOutF32;
         if (sp.a_mn) flags |= kFlagAmn;
         if (sp.b_mn) flags |= kFlagBmn;
+        if (sp.a_sym) {
+            flags |= kFlagAsym;
+            RET(operand(sp.A, 64u, pr.mAt, true));
+        }
+        if (sp.b_sym) {
+            flags |= kFlagBsym;
+            RET(operand(sp.B, 64u, pr.mBt, true));
+        }
+        if (sp.lower) flags |= kFlagLower;
         const bool share = ts_.np == 2 && (!sp.sym || share_symmetric());
         if (share) flags |= kFlagShareA;
         if (sp.C) {
@@ -523,8 +542,12 @@ Mat mat16(char* ws, size_t off, int rows, int cols, long long ld) {
 int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in,
              const MatrixSet* grads, float mu, int steps, int restart_at, const Coeffs& cf, const OutSpec& os,
              cudaStream_t s) {
-    ProgramBuilder prog(st, Gc, choose_tile(g.n), reinterpret_cast<int*>(st.ws + L.counters), s);
+    const TileShape ts = choose_tile(g.n);
+    ProgramBuilder prog(st, Gc, ts, reinterpret_cast<int*>(st.ws + L.counters), s);
     char* ws = st.ws;
+    // Symmetric n x n intermediates are stored lower-only (diagonal tiles in
+    // full) when the tiles are square.
+    const bool lo = ts.bn == 128 * ts.cg;
     const int n = g.n;
     // Stored copies of X in the input's orientation (R x C).
     Mat Xa = mat16(ws, L.xa, g.R, g.C, L.ld_x);
@@ -573,6 +596,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             pa.D = A;
             pa.Dt = &A;
             pa.sym = true;
+            pa.lower = lo;
             RET(phase(pa, nullptr));
             ProblemSpec pb;
             pb.A = A;
@@ -583,10 +607,12 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             pb.alpha = cf.c[t] * inv_s;
             pb.beta = cf.b[t];
             pb.sym = true;
+            pb.a_sym = pb.b_sym = pb.lower = lo;
             RET(phase(pb, nullptr));
             // X' = B X + a X: B is symmetric, X enters as the N x K operand X^T.
             ProblemSpec px;
             px.A = B;
+            px.a_sym = lo;
             xt_rows(px, false, X);
             px.C = &X;
             if (t + 1 < steps) {
@@ -620,16 +646,19 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
         p.D = R;
         p.Dt = &R;
         p.sym = true;
+        p.lower = lo;
         return phase(p, nullptr);
     };
     // Q X in the stored orientation: Q X (R <= C) or X^T Q = (Q X)^T (R > C).
     auto qx = [&](ProblemSpec& p) {
         if (!g.transposed) {
             p.A = Qc;
+            p.a_sym = lo;
             xt_rows(p, false, X);
         } else {
             xt_rows(p, true, X);
             p.B = Qc;
+            p.b_sym = lo;
         }
     };
     RET(gram());
@@ -658,6 +687,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             p.alpha = c * inv_s;
             p.beta = b;
             p.sym = true;
+            p.a_sym = p.b_sym = p.lower = lo;
             if (q_identity) {
                 p.D2 = &Qc;
                 p.D2t = &Qc;
@@ -676,6 +706,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             pq.alpha = inv_s;
             pq.beta = a;
             pq.sym = true;
+            pq.a_sym = pq.b_sym = pq.lower = lo;
         }
         if (need_r) {
             prz.A = R;
@@ -686,6 +717,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             prz.alpha = inv_s;
             prz.beta = a;
             prz.sym = true;
+            prz.a_sym = prz.b_sym = prz.lower = lo;
         }
         if (!q_identity && need_r) {
             RET(phase(pq, &prz));
@@ -706,6 +738,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             p.alpha = inv_s;
             p.beta = a;
             p.sym = true;
+            p.a_sym = p.b_sym = p.lower = lo;
             RET(phase(p, nullptr));
         }
     }

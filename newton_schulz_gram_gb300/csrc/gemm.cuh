@@ -29,8 +29,17 @@ enum GemmFlags : int {
     kFlagOutF32 = 16, // D is fp32 (otherwise fp16)
     kFlagAmn = 32,    // A is MN-major: the stored matrix is K x M (A^T row-major)
     kFlagBmn = 64,    // B is MN-major: the stored matrix is K x N (B^T row-major)
-    kFlagShareA = 128 // two CTA pairs of a cluster compute horizontally adjacent tiles
-                      // and share (multicast) their A operand
+    kFlagShareA = 128, // two CTA pairs of a cluster compute horizontally adjacent tiles
+                       // and share (multicast) their A operand
+    // Symmetric matrices stored lower-only: only tiles (I, J) with J <= I of
+    // a square tiling (edge = the tile's M edge, which then equals BN) hold
+    // data, diagonal tiles in full. An operand flagged so reads a k-block in
+    // tile column J > I as the transpose of tile (J, I) (an MN-major load
+    // through mAt / mBt); an output flagged kFlagLower is written that way
+    // (mirrored blocks only inside diagonal tiles).
+    kFlagAsym = 256,
+    kFlagBsym = 512,
+    kFlagLower = 1024
 };
 
 constexpr int kMaxMaps = 64;
@@ -52,6 +61,7 @@ struct GemmProblem {
     // 64 (K)}; both 128-byte swizzle. Output maps: box {32, 32}, 64-byte
     // swizzle (fp16) or 128-byte swizzle (fp32).
     int mA, mB, mD, mDt, mD2, mD2t;
+    int mAt, mBt;  // MN-major views (box {64, 64}) of lower-only A / B
 };
 
 struct GemmPhaseDesc {

@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     constexpr uint32_t A_BYTES = BM * BK * 2;
     constexpr uint32_t B_BYTES = BNH * BK * 2;
     constexpr uint32_t TMEM_COLS = 2 * BN;
-    constexpr uint32_t IDESC = idesc_f16_f32(BM * CG, BN);  // K-major; MN-major bits added per problem
+    constexpr uint32_t IDESC = idesc_f16_f32(BM * CG, BN);  // K-major; MN-major bits added per k-block
+    constexpr int TM = BM * CG;  // tile M edge; the storage tile of lower-only matrices
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -309,8 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const GemmProblem& pr = P.prob[t.p];
                 const CUtensorMap* mapA = &P.maps[pr.mA];
                 const CUtensorMap* mapB = &P.maps[pr.mB];
-                const bool a_mn = pr.flags & kFlagAmn;
-                const bool b_mn = pr.flags & kFlagBmn;
+                const bool a_mn0 = pr.flags & kFlagAmn;
+                const bool b_mn0 = pr.flags & kFlagBmn;
+                const bool a_sym = pr.flags & kFlagAsym;
+                const bool b_sym = pr.flags & kFlagBsym;
+                const CUtensorMap* mapAt = a_sym ? &P.maps[pr.mAt] : mapA;
+                const CUtensorMap* mapBt = b_sym ? &P.maps[pr.mBt] : mapB;
+                const int ti = t.m0 / TM, tj = t.n0 / TM;
                 const bool share = (NP == 2) && (pr.flags & kFlagShareA);
                 const int kblocks = (pr.K + BK - 1) / BK;
                 if (P.counters && P.phase[t.s].wait_tiles > 0) {
@@ -327,10 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     const uint32_t fb = full0 + 8 * stage;
                     const int arow = t.m0 + BM * static_cast<int>(rank);
                     const int brow = t.n0 + BNH * static_cast<int>(rank);
+                    // Lower-only operands: a k-block right of the diagonal tile is
+                    // read transposed from the tile below it.
+                    const int kt = (kb * BK) / TM;
+                    const bool a_t = a_sym && kt > ti;
+                    const bool b_t = b_sym && kt > tj;
+                    const bool a_mn = a_mn0 || a_t;
+                    const bool b_mn = b_mn0 || b_t;
+                    const CUtensorMap* mA_k = a_t ? mapAt : mapA;
+                    const CUtensorMap* mB_k = b_t ? mapBt : mapB;
                     if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-                        load_operand(0, smem_u32(sA + stage * A_BYTES), mapA, fb, a_mn, arow, BM, kb, t.g, 0);
-                        load_operand(0, smem_u32(sB + stage * B_BYTES), mapB, fb, b_mn, brow, BNH, kb, t.g, 0);
+                        load_operand(0, smem_u32(sA + stage * A_BYTES), mA_k, fb, a_mn, arow, BM, kb, t.g, 0);
+                        load_operand(0, smem_u32(sB + stage * B_BYTES), mB_k, fb, b_mn, brow, BNH, kb, t.g, 0);
                     } else {
                         // All halves complete on the pair leader's barrier. A
                         // shared A half is loaded once by the first pair and
@@ -338,13 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (A_BYTES + B_BYTES));
                         const uint32_t lead_fb = map_to_rank(fb, lead);
                         if (!share) {
-                            load_operand(1, smem_u32(sA + stage * A_BYTES), mapA, lead_fb, a_mn, arow, BM, kb, t.g, 0);
+                            load_operand(1, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g, 0);
                         } else if (pair == 0) {
                             const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2 + rank)));
-                            load_operand(2, smem_u32(sA + stage * A_BYTES), mapA, lead_fb, a_mn, arow, BM, kb, t.g,
+                            load_operand(2, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g,
                                          mask);
                         }
-                        load_operand(1, smem_u32(sB + stage * B_BYTES), mapB, lead_fb, b_mn, brow, BNH, kb, t.g, 0);
+                        load_operand(1, smem_u32(sB + stage * B_BYTES), mB_k, lead_fb, b_mn, brow, BNH, kb, t.g, 0);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -381,13 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const GemmProblem& pr = P.prob[t.p];
                 const int kblocks = (pr.K + BK - 1) / BK;
                 const int buf = iter & 1;
-                const uint32_t a_mn = (pr.flags & kFlagAmn) ? 1u : 0u;
-                const uint32_t b_mn = (pr.flags & kFlagBmn) ? 1u : 0u;
-                const uint32_t idesc = IDESC | (a_mn << 15) | (b_mn << 16);
-                // Per 16-wide k step: 32 bytes along a K-major row, or two
-                // 8-row groups (2048 bytes) of an MN-major tile.
-                const uint32_t a_step = a_mn ? (2048 >> 4) : (32 >> 4);
-                const uint32_t b_step = b_mn ? (2048 >> 4) : (32 >> 4);
+                const bool a_mn0 = pr.flags & kFlagAmn;
+                const bool b_mn0 = pr.flags & kFlagBmn;
+                const bool a_sym = pr.flags & kFlagAsym;
+                const bool b_sym = pr.flags & kFlagBsym;
+                const int ti = t.m0 / TM, tj = t.n0 / TM;
                 if (!mbar_wait(acce0 + 8 * buf, ((iter >> 1) & 1) ^ 1, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
@@ -397,6 +410,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     tc_fence_after();
+                    // The operand layouts the producer chose for this k-block.
+                    const int kt = (kb * BK) / TM;
+                    const uint32_t a_mn = (a_mn0 || (a_sym && kt > ti)) ? 1u : 0u;
+                    const uint32_t b_mn = (b_mn0 || (b_sym && kt > tj)) ? 1u : 0u;
+                    const uint32_t idesc = IDESC | (a_mn << 15) | (b_mn << 16);
+                    // Per 16-wide k step: 32 bytes along a K-major row, or two
+                    // 8-row groups (2048 bytes) of an MN-major tile.
+                    const uint32_t a_step = a_mn ? (2048 >> 4) : (32 >> 4);
+                    const uint32_t b_step = b_mn ? (2048 >> 4) : (32 >> 4);
                     const uint32_t sa = smem_u32(sA + stage * A_BYTES);
                     const uint32_t sb = smem_u32(sB + stage * B_BYTES);
                     const uint64_t adesc = a_mn ? sw128_mnmajor_desc(sa, kMnBlockBytes) : sw128_kmajor_desc(sa);
@@ -491,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                 }
                 const bool diag_block = sym && ((c0 >> 5) == sr);
-                const bool mirror = (flags & kFlagDt) && !diag_block;
+                // Lower-only outputs mirror only inside diagonal tiles.
+                const bool mirror = (flags & kFlagDt) && !diag_block && (!(flags & kFlagLower) || t.m0 == t.n0);
 
                 // Stage, transpose (mirror or diagonal fix-up) and store one
                 // 32 x 32 block; the buffer is free once the previous stores
