@@ -186,6 +186,29 @@ def cpu_threads():
     return os.cpu_count()
 
 
+def rank_seed(rank):
+    """Seed of a rank's bucket: every rank orthogonalizes its own independent
+    bucket (the matrices of a bucket are independent problems), so ranks
+    share no data and exchange nothing but timings."""
+    return 2000 + rank
+
+
+def max_over_ranks(value, dist, device):
+    """The job's time is its slowest rank's: max of a per-rank scalar over all
+    ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, seconds):
+    """Units processed by all ranks per second of the slowest rank."""
+    return units_per_rank * world / seconds
+
+
 def make_bucket(seed):
     from inputs import generators as gen
     return gen.gaussian_bucket(G, R, C, seed)
@@ -196,7 +219,7 @@ def run_reference(args, rank, world):
     the bucket in fp64 on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    bucket = make_bucket(2000)
+    bucket = make_bucket(rank_seed(0))
     import numpy as np
     from oracle import gram_ns
     for i in range(args.warmup):
@@ -250,7 +273,7 @@ def main():
     torch.cuda.set_device(dev)
     gns.load()
 
-    bucket = make_bucket(2000 + rank)
+    bucket = make_bucket(rank_seed(rank))
     host = torch.from_numpy(bucket).pin_memory()
     x = host.to(dev, non_blocking=False)
     stream = torch.cuda.current_stream(dev)
@@ -277,11 +300,7 @@ def main():
     e1.record(stream)
     barrier()
     launches = gns.gns_launch_count() - launches0
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
     # Same K steps again with per-launch events, for the per-kernel roofline.
     gns.gns_profile_enable(True)
@@ -304,15 +323,10 @@ def main():
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         gns.gns_orthogonalize_batched_host(hbuf, T_STEPS, RESTART)
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
 
     peaks = load_peaks()
-    total_matrices = G * args.steps * world
-    value = total_matrices / (ms / 1e3)
+    value = job_throughput(G * args.steps, world, ms / 1e3)
     per_step_s = ms / 1e3 / args.steps
     alg = G * alg_flops_per_matrix(R, C)
     eff = G * eff_flops_per_matrix(R, C)
@@ -341,7 +355,7 @@ def main():
         "kernels": kernels,
         "gpu_launches": launches,
         "clocks": sampler.summary(),
-        "e2e": {"value": G * e2e_steps * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": G * R * C * 4,
+        "e2e": {"value": job_throughput(G * e2e_steps, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": G * R * C * 4,
                 "d2h_bytes_per_step": G * R * C * 4},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
