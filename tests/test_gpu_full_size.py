@@ -125,3 +125,14 @@ def test_llama7b_muon_step(gns):
         noise = np.linalg.norm(np.abs(w_old) * 2.0 ** -7) * 2
         rel = np.linalg.norm(got_delta - want_delta) / np.linalg.norm(want_delta)
         assert rel <= 3e-2 + noise / np.linalg.norm(want_delta), (name, rel)
+
+
+def test_per_head_split_bucket(gns):
+    """An attention projection split by head (Dion3 App. A.1.1): W_Q of a
+    d = 4096 model with H = 16 heads becomes 16 matrices of 256 x 4096, whose
+    aspect ratio alpha = H makes the Gram form cheap. Every matrix against the
+    oracle."""
+    X = gen.gaussian_bucket(16, 256, 4096, seed=6000)
+    out = run_bucket(gns, X).cpu().numpy()
+    for g in range(X.shape[0]):
+        assert_parity(out[g], O.orthogonalize(X[g].astype(np.float64)), what=f"head {g}")
