@@ -235,6 +235,7 @@ struct ProblemSpec {
     // Lower-only storage of symmetric matrices (square tile shapes only):
     // A / B are read that way, D (and D2) are written that way.
     bool a_sym = false, b_sym = false, lower = false;
+    const MuonFuse* muon = nullptr;  // fused Muon update instead of storing D
 };
 
 // Tile shape for a program: 256 x 256 tiles on CTA pairs (two pairs per
@@ -372,7 +373,12 @@ class ProgramBuilder {
         if ((sp.a_sym && sp.a_mn) || (sp.b_sym && sp.b_mn)) return fail(GNS_ERR_INVALID, "lower-only operands are K-major");
         RET(operand(sp.A, sp.a_mn ? 64u : 128u, pr.mA, sp.a_mn));
         RET(operand(sp.B, sp.b_mn ? 64u : static_cast<uint32_t>(bn / cg), pr.mB, sp.b_mn));
-        RET(output(sp.D, pr.mD));
+        if (sp.muon) {
+            if (sp.sym || sp.Dt || sp.D2) return fail(GNS_ERR_INVALID, "the fused update needs a plain product");
+            pr.muon = *sp.muon;
+        } else {
+            RET(output(sp.D, pr.mD));
+        }
         int flags = 0;
         if (sp.sym) flags |= kFlagSym;
         if (sp.D.f32) flags |= kFlagOutF32;
@@ -387,6 +393,7 @@ class ProgramBuilder {
             RET(operand(sp.B, 64u, pr.mBt, true));
         }
         if (sp.lower) flags |= kFlagLower;
+        if (sp.muon) flags |= kFlagMuon;
         const bool share = ts_.np == 2 && (!sp.sym || share_symmetric());
         if (share) flags |= kFlagShareA;
         if (sp.C) {
@@ -461,6 +468,7 @@ bool is_restart_after(int t, int steps, int restart_at) {
 // Where the result of one bucket goes.
 struct OutSpec {
     Mat out;        // fp32 [G][R][C] (ABI) or fp16 [G][R][ld] (Muon O)
+    const MuonFuse* muon = nullptr;  // set: the last product updates W instead of storing out
     bool copy_back = false;  // out is a workspace buffer; copy to user_ptr afterwards
     float* user_ptr = nullptr;
 };
@@ -623,6 +631,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
                 std::swap(X, Xn);
             } else {
                 px.D = os.out;
+                px.muon = os.muon;
                 px.alpha = inv_s * out_scale;
                 px.beta = cf.a[t] * out_scale;
                 RET(phase(px, nullptr));
@@ -746,6 +755,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     ProblemSpec p;
     qx(p);
     p.D = os.out;
+    p.muon = os.muon;
     p.alpha = out_scale;
     RET(phase(p, nullptr));
     return prog.flush();
@@ -858,6 +868,14 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
     return GNS_OK;
 }
 
+// The Muon update runs in the epilogue of the last product (the default), or
+// as a separate pass over a stored fp16 O when GNS_MUON_FUSED=0; both give
+// identical bits.
+bool muon_fused() {
+    const char* e = std::getenv("GNS_MUON_FUSED");
+    return !(e && std::string(e) == "0");
+}
+
 int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n, float lr,
               float wd, float mu, uint64_t seed, uint64_t step, void* stream) {
     if (n < 0) return fail(GNS_ERR_INVALID, "n < 0");
@@ -891,9 +909,10 @@ int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tenso
         const int R = bk.first.first, C = bk.first.second;
         const int G = static_cast<int>(bk.second.size());
         const BucketGeom g = make_geom(R, C);
-        const int Gc = chunk_size(g, G, false, true);
+        const bool fused = muon_fused();
+        const int Gc = chunk_size(g, G, false, !fused);
         const size_t meta_bytes = static_cast<size_t>(Gc) * (3 * sizeof(void*) + sizeof(long long)) + 256;
-        const Layout L = make_layout(g, Gc, false, true, meta_bytes);
+        const Layout L = make_layout(g, Gc, false, !fused, meta_bytes);
         RET(ensure_workspace(*st, L.total));
         const long long numel = static_cast<long long>(R) * C;
         const long long ld_o = round_up_ll(C, 8);
@@ -918,15 +937,32 @@ int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tenso
             MatrixSet Gs{nullptr, 0, pm + gc};
             MatrixSet Ws{nullptr, 0, pm + 2 * gc};
             OutSpec os;
-            os.out.p = st->ws + L.o16;
             os.out.rows = R;
             os.out.cols = C;
-            os.out.ld = ld_o;
-            os.out.stride = static_cast<long long>(R) * ld_o;
             os.out.f32 = false;
+            MuonFuse mf{};
+            if (fused) {
+                mf.w = reinterpret_cast<uint16_t* const*>(meta) + 2 * gc;
+                mf.base = bases_dev;
+                mf.lr = lr;
+                mf.wd = wd;
+                mf.scale = scale;
+                mf.seed_lo = static_cast<uint32_t>(seed);
+                mf.seed_hi = static_cast<uint32_t>(seed >> 32);
+                mf.step_lo = static_cast<uint32_t>(step);
+                mf.step_hi = static_cast<uint32_t>(step >> 32);
+                os.muon = &mf;
+            } else {
+                os.out.p = st->ws + L.o16;
+                os.out.ld = ld_o;
+                os.out.stride = static_cast<long long>(R) * ld_o;
+            }
             RET(run_core(*st, g, L, gc, Ms, &Gs, mu, 5, 2, cf, os, s));
-            MatrixSet Os{os.out.p, os.out.stride, nullptr};
-            LAUNCH(kClsMuon, launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s));
+            if (!fused) {
+                MatrixSet Os{os.out.p, os.out.stride, nullptr};
+                LAUNCH(kClsMuon,
+                       launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s));
+            }
         }
     }
     return GNS_OK;

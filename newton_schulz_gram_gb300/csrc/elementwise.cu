@@ -20,6 +20,7 @@
 #include <cstdlib>
 
 #include "elementwise.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace gns {
@@ -447,33 +448,6 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(MatrixSet Ms, Matrix
     if (beg < end)
         momentum_range<kThreads>(mat_ptr<float>(Ms, g), mat_ptr<const __nv_bfloat16>(Gs, g), beg, end, mu,
                                  threadIdx.x);
-}
-
-__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        if (r > 0) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c[0]);
-        const uint32_t lo0 = 0xD2511F53u * c[0];
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c[2]);
-        const uint32_t lo1 = 0xCD9E8D57u * c[2];
-        const uint32_t n0 = hi1 ^ c[1] ^ k0;
-        const uint32_t n2 = hi0 ^ c[3] ^ k1;
-        c[0] = n0;
-        c[1] = lo1;
-        c[2] = n2;
-        c[3] = lo0;
-    }
-}
-
-__device__ __forceinline__ uint16_t sr_bf16(float w, uint32_t u16) {
-    const uint32_t b = __float_as_uint(w);
-    if ((b & 0x7F800000u) == 0x7F800000u)
-        return static_cast<uint16_t>((b & 0x007FFFFFu) ? ((b >> 16) | 0x40u) : (b >> 16));
-    return static_cast<uint16_t>((b + u16) >> 16);
 }
 
 // One thread per group of 4 global indices g = 4 blk .. 4 blk + 3.

@@ -39,7 +39,20 @@ enum GemmFlags : int {
     // (mirrored blocks only inside diagonal tiles).
     kFlagAsym = 256,
     kFlagBsym = 512,
-    kFlagLower = 1024
+    kFlagLower = 1024,
+    // Fused Muon update: D is not stored; each output element o = fp16(alpha
+    // acc) updates the bf16 weight of the same (row, column) of matrix g,
+    // W <- SR_bf16((1 - lr wd) W - (lr scale) o), with the stochastic
+    // rounding counter of global index w_base[g] + row N + column.
+    kFlagMuon = 2048
+};
+
+// Parameters of the fused Muon update (kFlagMuon).
+struct MuonFuse {
+    uint16_t* const* w;     // device array [G]: bf16 W, row-major M x N, contiguous
+    const long long* base;  // device array [G]: global index of each W's first element
+    float lr, wd, scale;
+    uint32_t seed_lo, seed_hi, step_lo, step_hi;
 };
 
 constexpr int kMaxMaps = 64;
@@ -62,6 +75,7 @@ struct GemmProblem {
     // swizzle (fp16) or 128-byte swizzle (fp32).
     int mA, mB, mD, mDt, mD2, mD2t;
     int mAt, mBt;  // MN-major views (box {64, 64}) of lower-only A / B
+    MuonFuse muon;
 };
 
 struct GemmPhaseDesc {

@@ -29,6 +29,7 @@
 #include <cstdio>
 
 #include "gemm.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace gns {
@@ -217,6 +218,58 @@ __device__ __forceinline__ void load_c(const GemmProblem& pr, int g, int grow, i
         for (int k = 0; k < 4; ++k)
             cb[k] = make_uint4(h[8 * k] | (uint32_t(h[8 * k + 1]) << 16), h[8 * k + 2] | (uint32_t(h[8 * k + 3]) << 16),
                                h[8 * k + 4] | (uint32_t(h[8 * k + 5]) << 16), h[8 * k + 6] | (uint32_t(h[8 * k + 7]) << 16));
+    }
+}
+
+// Fused Muon update of one output row segment: columns c0 .. c0 + 31 of row
+// `row` of matrix g, whose output values (alpha acc) are v. Each value is
+// rounded to fp16 first (the value the unfused path stores and reads back),
+// so the result equals the separate update kernel's bit for bit.
+__device__ __forceinline__ void muon_update_row(const GemmProblem& pr, int g, int row, int c0, const float (&v)[32]) {
+    if (row >= pr.M || c0 >= pr.N) return;
+    const MuonFuse& mf = pr.muon;
+    const float decay = __fsub_rn(1.0f, __fmul_rn(mf.lr, mf.wd));
+    const float stepv = __fmul_rn(mf.lr, mf.scale);
+    const long long i0 = static_cast<long long>(row) * pr.N + c0;
+    const unsigned long long g0 = static_cast<unsigned long long>(mf.base[g] + i0);
+    uint16_t* wp = mf.w[g] + i0;
+    const int ncol = pr.N - c0 < 32 ? pr.N - c0 : 32;
+    auto upd = [&](uint16_t wbits, float acc, uint32_t u) -> uint16_t {
+        const float o = __half2float(__float2half_rn(acc));
+        const float w = __uint_as_float(static_cast<uint32_t>(wbits) << 16);
+        const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
+        return sr_bf16(wn, u & 0xFFFFu);
+    };
+    if (ncol == 32 && (g0 & 3) == 0 && (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
+        uint4 wv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) wv[k] = reinterpret_cast<const uint4*>(wp)[k];
+        uint16_t* wh = reinterpret_cast<uint16_t*>(wv);
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const unsigned long long blk = (g0 >> 2) + b;
+            uint32_t c[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), mf.step_lo, mf.step_hi};
+            philox4x32_10(c, mf.seed_lo, mf.seed_hi);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) wh[4 * b + e] = upd(wh[4 * b + e], v[4 * b + e], c[e]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(wp)[k] = wv[k];
+    } else {
+        unsigned long long cur = ~0ULL;
+        uint32_t c[4] = {0, 0, 0, 0};
+        for (int j = 0; j < ncol; ++j) {
+            const unsigned long long gi = g0 + j;
+            if ((gi >> 2) != cur) {
+                cur = gi >> 2;
+                c[0] = static_cast<uint32_t>(cur);
+                c[1] = static_cast<uint32_t>(cur >> 32);
+                c[2] = mf.step_lo;
+                c[3] = mf.step_hi;
+                philox4x32_10(c, mf.seed_lo, mf.seed_hi);
+            }
+            wp[j] = upd(wp[j], v[j], c[gi & 3]);
+        }
     }
 }
 
@@ -511,6 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                             v[8 * k + 2 * e + 1] = fmaf(pr.beta, f.y, v[8 * k + 2 * e + 1]);
                         }
                     }
+                }
+                if (flags & kFlagMuon) {
+                    muon_update_row(pr, t.g, grow, c0, v);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) cb[k] = cbn[k];
+                    c = cn;
+                    continue;
                 }
                 const bool diag_block = sym && ((c0 >> 5) == sr);
                 // Lower-only outputs mirror only inside diagonal tiles.
