@@ -15,6 +15,13 @@ What it computes:
   decay = 1 - lr*wd; step = lr*s; w' = decay*w - step*o.
 * Scale s = 0.2 * sqrt(max(rows, cols)): the Moonshot rule that Dion3 App. A.1
   reports as the best for its Muon runs.
+* NorMuon flavor (Dion3 §2.1, Eq. 2): after O = polar(M), per row i of the
+  weight's shape, v_i <- beta2 v_i + (1 - beta2) (1/m) sum_j O_ij^2 with m the
+  number of columns; O^_ij = O_ij / (sqrt(v_i) + eps); the update direction is
+  O^ rescaled to the Frobenius norm of O. Readings: the same decoupled weight
+  decay and scale s as the Muon flavor apply on top (Dion3 §6 applies weight
+  decay before either flavor's update); v starts at zero and is the caller's
+  state like M. Computed in fp64 here (Dion3 §6 asks for at least fp32).
 * Stochastic rounding of w' to bf16, keyed by the element's global index
   (the grouped Muon kernel card: "counter-based stochastic rounding keyed by
   the element's global index", "base_index sets the global-index offset").
@@ -151,3 +158,39 @@ def muon_step(params_bits, grads_bits, momenta, lr, wd, mu, seed, step,
         new_m.append(m_new)
         outs.append(o)
     return new_w, new_m, outs
+
+
+def normuon_normalize(O, v, beta2, eps):
+    """NorMuon's steps after the orthogonalization (Dion3 Eq. 2), in fp64:
+    returns (U, v_new) with v_new_i = beta2 v_i + (1 - beta2) mean_j O_ij^2,
+    O^ = O / (sqrt(v_new) + eps) row by row, and U = (||O||_F / ||O^||_F) O^
+    (zero when O^ is zero)."""
+    O = np.asarray(O, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    m = O.shape[1]
+    v_new = beta2 * v + (1.0 - beta2) * np.sum(O * O, axis=1) / m
+    O_hat = O / (np.sqrt(v_new) + eps)[:, None]
+    n_o, n_hat = np.linalg.norm(O), np.linalg.norm(O_hat)
+    U = O_hat * (n_o / n_hat) if n_hat > 0 else np.zeros_like(O_hat)
+    return U, v_new
+
+
+def normuon_step(params_bits, grads_bits, momenta, second_moments, lr, wd, mu, beta2, eps, seed, step,
+                 base_indices=None, ns=None):
+    """A full NorMuon step over a list of matrices (Dion3 Eq. 2 with the Muon
+    flavor's decoupled weight decay, scale and stochastic rounding). Returns
+    (new param bits, new momenta, new second moments, update directions U)."""
+    from .gram_ns import orthogonalize
+    ns = ns or orthogonalize
+    if base_indices is None:
+        base_indices = [0] * len(params_bits)
+    new_w, new_m, new_v, dirs = [], [], [], []
+    for w_bits, g_bits, m, v, base in zip(params_bits, grads_bits, momenta, second_moments, base_indices):
+        m_new = momentum(m, bf16_bits_to_f32(g_bits), mu)
+        U, v_new = normuon_normalize(ns(m_new.astype(np.float64)), v, beta2, eps)
+        s = update_scale(*w_bits.shape)
+        new_w.append(muon_update_bf16(w_bits, U.astype(np.float32), lr, wd, s, seed, step, base))
+        new_m.append(m_new)
+        new_v.append(v_new)
+        dirs.append(U)
+    return new_w, new_m, new_v, dirs

@@ -6,6 +6,8 @@ import os
 import numpy as np
 import pytest
 
+from inputs import generators as gen
+from oracle import gram_ns as O_NS
 from oracle import muon as MU
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -125,3 +127,78 @@ def test_muon_step_matches_definition():
     # Stochastic rounding moves each element by less than one bf16 ULP.
     ulp = np.abs(want) * 2.0 ** -7 + 1e-30
     assert np.all(np.abs(w_new - want) <= ulp)
+
+
+# ---------------------------------------------------------------- NorMuon
+# Pins of Dion3 Eq. 2 (NorMuon): the second moment's recursion, the row
+# balance it produces, the Frobenius rescale, and its reduction to Muon when
+# the rows of O already have equal norms.
+
+def _rows_with_scales(R, C, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((R, C)) * np.exp(rng.uniform(-3, 3, size=(R, 1)))
+
+
+def test_normuon_second_moment_recursion():
+    O = _rows_with_scales(6, 10, 1)
+    v0 = np.random.default_rng(2).uniform(0, 1, 6)
+    _, v1 = MU.normuon_normalize(O, v0, 0.9, 1e-8)
+    want = 0.9 * v0 + 0.1 * np.array([np.dot(r, r) / 10 for r in O])  # mean over the m = 10 columns
+    assert np.allclose(v1, want, rtol=1e-14)
+    _, vz = MU.normuon_normalize(np.zeros((6, 10)), v0, 0.9, 1e-8)
+    assert np.allclose(vz, 0.9 * v0, rtol=1e-15)
+
+
+def test_normuon_balances_rows_and_keeps_the_frobenius_norm():
+    O = _rows_with_scales(8, 24, 3)
+    U, _ = MU.normuon_normalize(O, np.zeros(8), 0.0, 0.0)
+    # beta2 = 0, eps = 0: v_i is the mean square of row i, so every row of O^
+    # has unit RMS and every row of U the same norm ||O|| / sqrt(R).
+    row_norms = np.linalg.norm(U, axis=1)
+    assert np.allclose(row_norms, np.linalg.norm(O) / np.sqrt(8), rtol=1e-12)
+    assert np.isclose(np.linalg.norm(U), np.linalg.norm(O), rtol=1e-14)
+    assert np.all(np.sign(U) == np.sign(O))  # a positive scale per row
+    # The columns are not balanced (normalizing columns instead would be).
+    col_norms = np.linalg.norm(U, axis=0)
+    assert col_norms.std() / col_norms.mean() > 1e-2
+    # Any beta2 and eps keep the Frobenius norm.
+    U2, _ = MU.normuon_normalize(O, np.random.default_rng(4).uniform(0, 2, 8), 0.95, 1e-3)
+    assert np.isclose(np.linalg.norm(U2), np.linalg.norm(O), rtol=1e-14)
+
+
+def test_normuon_equals_muon_for_equal_row_norms():
+    """An input with orthonormal rows normalizes to kappa X (all normalized
+    singular values equal), so O has equal row norms and NorMuon's direction
+    is exactly O: NorMuon reduces to Muon."""
+    X = gen.orthonormal_rows_matrix(16, 64, seed=5, dtype=np.float64)
+    O = O_NS.orthogonalize(X)
+    U, _ = MU.normuon_normalize(O, np.zeros(16), 0.95, 1e-8)
+    assert np.allclose(U, O, rtol=1e-12, atol=1e-14)
+
+
+def test_normuon_step_composes_the_pieces():
+    R, C = 12, 40
+    w, g = gen.muon_param_inputs(R, C, seed=8, index=0)
+    w_bits, g_bits = MU.f32_to_bf16_rne_bits(w), MU.f32_to_bf16_rne_bits(g)
+    m0 = np.zeros((R, C), np.float32)
+    v0 = np.zeros(R)
+    new_w, new_m, new_v, dirs = MU.normuon_step([w_bits], [g_bits], [m0], [v0], 0.02, 0.01, 0.9, 0.95, 1e-8,
+                                                seed=1, step=3, base_indices=[77])
+    m1 = MU.momentum(m0, MU.bf16_bits_to_f32(g_bits), 0.9)
+    U, v1 = MU.normuon_normalize(O_NS.orthogonalize(m1.astype(np.float64)), v0, 0.95, 1e-8)
+    assert np.array_equal(new_m[0], m1)
+    assert np.allclose(new_v[0], v1) and np.allclose(dirs[0], U)
+    want = MU.muon_update_bf16(w_bits, U.astype(np.float32), 0.02, 0.01, MU.update_scale(R, C), 1, 3, 77)
+    assert np.array_equal(new_w[0], want)
+
+
+def test_normuon_eps_outside_the_square_root():
+    """Row i of U is O_i / (sqrt(v_i) + eps) times one common factor: with a
+    large eps the ratio of two rows' scales pins where eps enters."""
+    O = np.array([[3.0, 4.0, 0.0], [0.0, 0.6, 0.8]])
+    eps = 0.5
+    U, v = MU.normuon_normalize(O, np.zeros(2), 0.0, eps)
+    assert np.allclose(v, [25.0 / 3, 1.0 / 3], rtol=1e-15)
+    scale = np.linalg.norm(U, axis=1) / np.linalg.norm(O, axis=1)
+    want = (np.sqrt(v[1]) + eps) / (np.sqrt(v[0]) + eps)
+    assert np.isclose(scale[0] / scale[1], want, rtol=1e-14)

@@ -97,3 +97,44 @@ def test_mutant_is_caught(name):
     old, new = MUTANTS[name]
     assert src.count(old) == 1, f"mutation site not unique/found: {name}"
     assert not pins_pass(load_variant(f"oracle_{name}", src.replace(old, new)))
+
+
+# NorMuon (Dion3 Eq. 2) in oracle/muon.py: the same check against its pins.
+MU_SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "muon.py")
+
+NORMUON_MUTANTS = {
+    "normuon_mean_over_rows": ("np.sum(O * O, axis=1) / m", "np.sum(O * O, axis=1) / O.shape[0]"),
+    "normuon_drop_one_minus_beta2": ("(1.0 - beta2) * np.sum(O * O, axis=1)", "np.sum(O * O, axis=1)"),
+    "normuon_eps_inside_sqrt": ("(np.sqrt(v_new) + eps)", "np.sqrt(v_new + eps)"),
+    "normuon_no_rescale": ("U = O_hat * (n_o / n_hat) if n_hat > 0", "U = O_hat if n_hat > 0"),
+    "normuon_rescale_inverted": ("U = O_hat * (n_o / n_hat) if n_hat > 0", "U = O_hat * (n_hat / n_o) if n_hat > 0"),
+    "normuon_columns": ("O_hat = O / (np.sqrt(v_new) + eps)[:, None]",
+                        "O_hat = (O.T / (np.sqrt(v_new) + eps)[: O.shape[1], None]).T"),
+}
+
+
+def normuon_pins_pass(MU):
+    import tests.test_oracle_muon as T
+    saved = T.MU
+    T.MU = MU
+    try:
+        for fn in (T.test_normuon_second_moment_recursion, T.test_normuon_balances_rows_and_keeps_the_frobenius_norm,
+                   T.test_normuon_equals_muon_for_equal_row_norms, T.test_normuon_eps_outside_the_square_root):
+            fn()
+    except Exception:
+        return False
+    finally:
+        T.MU = saved
+    return True
+
+
+def test_normuon_original_passes():
+    assert normuon_pins_pass(load_variant("muon_original", open(MU_SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(NORMUON_MUTANTS))
+def test_normuon_mutant_is_caught(name):
+    src = open(MU_SRC).read()
+    old, new = NORMUON_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site not unique/found: {name}"
+    assert not normuon_pins_pass(load_variant(f"muon_{name}", src.replace(old, new)))
