@@ -141,6 +141,24 @@ int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tenso
               int n, float lr, float wd, float mu, uint64_t seed, uint64_t step, void* stream);
 
 /*
+ * normuon_step: one NorMuon step (Dion3 §2.1 Eq. 2) over n weight matrices:
+ * muon_step's momentum and orthogonalization, then, per row i of O (the
+ * weight's own rows), in fp32:
+ *   v_i <- beta2 v_i + (1 - beta2) (1/cols) sum_j O_ij^2
+ *   U   =  (||O||_F / ||O^||_F) O^,   O^_ij = O_ij / (sqrt(v_i) + eps)
+ *   W   <- SR_bf16((1 - lr*wd) W - lr*s*U),  s = 0.2 sqrt(max(rows, cols))
+ * with the stochastic rounding of muon_step. The row statistics and the two
+ * norms are summed in a fixed order, so results do not depend on the
+ * bucketing.
+ *   second_moments  n tensors, fp32 v, each rows x 1 (the weight's rows),
+ *                   updated in place; start them at zero.
+ * Other arguments as muon_step; beta2 in [0, 1], eps >= 0.
+ */
+int normuon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum,
+                 const gns_tensor* second_moments, int n, float lr, float wd, float mu, float beta2,
+                 float eps, uint64_t seed, uint64_t step, void* stream);
+
+/*
  * gns_muon_momentum: the first elementwise pass of muon_step on one tensor:
  * M <- mu*M + float(G), fp32, two roundings (Dion3 Eq. 1).
  *   M      device fp32 [numel], updated in place.

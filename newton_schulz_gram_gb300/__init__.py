@@ -14,7 +14,7 @@ import torch
 from ._lib import GnsError, GnsTensor, check, load
 
 __all__ = ["gns_orthogonalize_batched", "gns_orthogonalize_batched_host",
-           "gns_orthogonalize_batched_noalloc", "muon_step",
+           "gns_orthogonalize_batched_noalloc", "muon_step", "normuon_step",
            "gns_muon_momentum", "gns_muon_update", "gns_symm_gemm", "gns_get_status",
            "gns_status_string", "gns_last_error", "gns_workspace_bytes", "gns_release",
            "gns_launch_count", "gns_profile_enable", "gns_profile_read", "KERNEL_CLASSES",
@@ -122,6 +122,29 @@ def muon_step(params, grads, momenta, lr, wd, mu, seed, step, base_indices=None,
     M = _tensors(momenta, torch.float32, "momenta")
     lib = load()
     check(lib.muon_step(P, Gr, M, n, lr, wd, mu, seed, step, _stream(stream, params[0].device)), "muon_step")
+
+
+def normuon_step(params, grads, momenta, second_moments, lr, wd, mu, beta2=0.95, eps=1e-8, seed=0, step=0,
+                 base_indices=None, stream=None):
+    """One NorMuon step (Dion3 Eq. 2): as muon_step, plus the per-row fp32
+    second moments (one float per row of each param, updated in place)."""
+    n = len(params)
+    if len(grads) != n or len(momenta) != n or len(second_moments) != n:
+        raise ValueError("params, grads, momenta and second_moments must have equal lengths")
+    if n == 0:
+        return
+    if base_indices is None:
+        base_indices, acc = [], 0
+        for p in params:
+            base_indices.append(acc)
+            acc += p.numel()
+    P = _tensors(params, torch.bfloat16, "params", base_indices)
+    Gr = _tensors(grads, torch.bfloat16, "grads")
+    M = _tensors(momenta, torch.float32, "momenta")
+    V = _tensors([v.view(-1, 1) for v in second_moments], torch.float32, "second_moments")
+    lib = load()
+    check(lib.normuon_step(P, Gr, M, V, n, lr, wd, mu, beta2, eps, seed, step, _stream(stream, params[0].device)),
+          "normuon_step")
 
 
 def gns_muon_momentum(M, G, mu, stream=None):

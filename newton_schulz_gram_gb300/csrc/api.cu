@@ -827,6 +827,132 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart
     return GNS_OK;
 }
 
+// The Muon update runs in the epilogue of the last product (the default), or
+// as a separate pass over a stored fp16 O when GNS_MUON_FUSED=0; both give
+// identical bits.
+bool muon_fused() {
+    const char* e = std::getenv("GNS_MUON_FUSED");
+    return !(e && std::string(e) == "0");
+}
+
+// One Muon (vm == nullptr) or NorMuon step over n matrices, bucketed by shape.
+int optimizer_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum,
+                   const gns_tensor* vm, int n, float lr, float wd, float mu, float beta2, float eps, uint64_t seed,
+                   uint64_t step, void* stream) {
+    if (n < 0) return fail(GNS_ERR_INVALID, "n < 0");
+    if (n == 0) return GNS_OK;
+    if (!params || !grads || !momentum) return fail(GNS_ERR_INVALID, "null tensor array");
+    for (int i = 0; i < n; ++i) {
+        const gns_tensor &w = params[i], &gr = grads[i], &mm = momentum[i];
+        if (!w.data || !gr.data || !mm.data) return fail(GNS_ERR_INVALID, "null tensor data");
+        if (w.rows < 1 || w.cols < 1 || gr.rows != w.rows || gr.cols != w.cols || mm.rows != w.rows ||
+            mm.cols != w.cols)
+            return fail(GNS_ERR_INVALID, "tensor shapes differ");
+        if (w.base_index < 0) return fail(GNS_ERR_INVALID, "negative base_index");
+        if (vm && (!vm[i].data || vm[i].rows != w.rows || vm[i].cols != 1))
+            return fail(GNS_ERR_INVALID, "second moments must be rows x 1");
+    }
+    if (vm && !(beta2 >= 0.0f && beta2 <= 1.0f && eps >= 0.0f)) return fail(GNS_ERR_INVALID, "bad beta2 or eps");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    // Buckets of equal (rows, cols), in order of first appearance.
+    std::vector<std::pair<std::pair<int, int>, std::vector<int>>> buckets;
+    for (int i = 0; i < n; ++i) {
+        auto key = std::make_pair(params[i].rows, params[i].cols);
+        auto it = std::find_if(buckets.begin(), buckets.end(), [&](const auto& b) { return b.first == key; });
+        if (it == buckets.end()) {
+            buckets.push_back({key, {i}});
+        } else {
+            it->second.push_back(i);
+        }
+    }
+    Coeffs cf;
+    RET(load_coeffs(nullptr, 5, cf));
+    const int narr = vm ? 4 : 3;  // pointer arrays: M, G, W (, V)
+    for (auto& bk : buckets) {
+        const int R = bk.first.first, C = bk.first.second;
+        const int G = static_cast<int>(bk.second.size());
+        const BucketGeom g = make_geom(R, C);
+        // NorMuon needs all of O before its row statistics: it stores O.
+        const bool fused = !vm && muon_fused();
+        const size_t per_matrix_meta = narr * sizeof(void*) + sizeof(long long) + (vm ? 4 * sizeof(float) * R : 0);
+        int Gc = chunk_size(g, G, false, !fused);
+        // The statistics buffers live in the metadata block.
+        while (Gc > 1 && make_layout(g, Gc, false, !fused, static_cast<size_t>(Gc) * per_matrix_meta + 1024).total >
+                             chunk_cap_bytes())
+            --Gc;
+        const size_t meta_bytes = static_cast<size_t>(Gc) * per_matrix_meta + 1024;
+        const Layout L = make_layout(g, Gc, false, !fused, meta_bytes);
+        RET(ensure_workspace(*st, L.total));
+        const long long ld_o = round_up_ll(C, 8);
+        const float scale = 0.2f * std::sqrt(static_cast<float>(std::max(R, C)));
+        for (int g0 = 0; g0 < G; g0 += Gc) {
+            const int gc = std::min(Gc, G - g0);
+            std::vector<const void*> ptrs(narr * static_cast<size_t>(gc));
+            std::vector<long long> bases(gc);
+            for (int j = 0; j < gc; ++j) {
+                const int i = bk.second[g0 + j];
+                ptrs[j] = momentum[i].data;
+                ptrs[gc + j] = grads[i].data;
+                ptrs[2 * gc + j] = params[i].data;
+                if (vm) ptrs[3 * gc + j] = vm[i].data;
+                bases[j] = params[i].base_index;
+            }
+            char* meta = st->ws + L.meta;
+            CK(cudaMemcpyAsync(meta, ptrs.data(), ptrs.size() * sizeof(void*), cudaMemcpyHostToDevice, s));
+            long long* bases_dev = reinterpret_cast<long long*>(meta + align_up(ptrs.size() * sizeof(void*), 16));
+            CK(cudaMemcpyAsync(bases_dev, bases.data(), bases.size() * sizeof(long long), cudaMemcpyHostToDevice, s));
+            float* stats = reinterpret_cast<float*>(
+                meta + align_up(align_up(ptrs.size() * sizeof(void*), 16) + bases.size() * sizeof(long long), 256));
+            const void* const* pm = reinterpret_cast<const void* const*>(meta);
+            MatrixSet Ms{nullptr, 0, pm};
+            MatrixSet Gs{nullptr, 0, pm + gc};
+            MatrixSet Ws{nullptr, 0, pm + 2 * gc};
+            OutSpec os;
+            os.out.rows = R;
+            os.out.cols = C;
+            os.out.f32 = false;
+            MuonFuse mf{};
+            if (fused) {
+                mf.w = reinterpret_cast<uint16_t* const*>(meta) + 2 * gc;
+                mf.base = bases_dev;
+                mf.lr = lr;
+                mf.wd = wd;
+                mf.scale = scale;
+                mf.seed_lo = static_cast<uint32_t>(seed);
+                mf.seed_hi = static_cast<uint32_t>(seed >> 32);
+                mf.step_lo = static_cast<uint32_t>(step);
+                mf.step_hi = static_cast<uint32_t>(step >> 32);
+                os.muon = &mf;
+            } else {
+                os.out.p = st->ws + L.o16;
+                os.out.ld = ld_o;
+                os.out.stride = static_cast<long long>(R) * ld_o;
+            }
+            RET(run_core(*st, g, L, gc, Ms, &Gs, mu, 5, 2, cf, os, s));
+            if (fused) continue;
+            MatrixSet Os{os.out.p, os.out.stride, nullptr};
+            const float* row_step = nullptr;
+            if (vm) {
+                // Dion3 Eq. 2: row second moments, then one factor per matrix.
+                MatrixSet Vs{nullptr, 0, pm + 3 * gc};
+                const size_t rc = static_cast<size_t>(gc) * R;
+                float* row_sq = stats;
+                float* row_hat = stats + rc;
+                float* inv = stats + 2 * rc;
+                float* steps = stats + 3 * rc;
+                LAUNCH(kClsMuon, launch_normuon_rows(Os, ld_o, Vs, gc, R, C, beta2, eps, row_sq, row_hat, inv, s));
+                LAUNCH(kClsMuon, launch_normuon_factor(row_sq, row_hat, inv, gc, R, lr * scale, steps, s));
+                row_step = steps;
+            }
+            LAUNCH(kClsMuon, launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s,
+                                                row_step));
+        }
+    }
+    return GNS_OK;
+}
+
 }  // namespace
 }  // namespace gns
 
@@ -868,104 +994,16 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
     return GNS_OK;
 }
 
-// The Muon update runs in the epilogue of the last product (the default), or
-// as a separate pass over a stored fp16 O when GNS_MUON_FUSED=0; both give
-// identical bits.
-bool muon_fused() {
-    const char* e = std::getenv("GNS_MUON_FUSED");
-    return !(e && std::string(e) == "0");
-}
-
 int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n, float lr,
               float wd, float mu, uint64_t seed, uint64_t step, void* stream) {
-    if (n < 0) return fail(GNS_ERR_INVALID, "n < 0");
-    if (n == 0) return GNS_OK;
-    if (!params || !grads || !momentum) return fail(GNS_ERR_INVALID, "null tensor array");
-    for (int i = 0; i < n; ++i) {
-        const gns_tensor &w = params[i], &gr = grads[i], &mm = momentum[i];
-        if (!w.data || !gr.data || !mm.data) return fail(GNS_ERR_INVALID, "null tensor data");
-        if (w.rows < 1 || w.cols < 1 || gr.rows != w.rows || gr.cols != w.cols || mm.rows != w.rows ||
-            mm.cols != w.cols)
-            return fail(GNS_ERR_INVALID, "tensor shapes differ");
-        if (w.base_index < 0) return fail(GNS_ERR_INVALID, "negative base_index");
-    }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    DeviceState* st = nullptr;
-    RET(get_state(&st));
-    // Buckets of equal (rows, cols), in order of first appearance.
-    std::vector<std::pair<std::pair<int, int>, std::vector<int>>> buckets;
-    for (int i = 0; i < n; ++i) {
-        auto key = std::make_pair(params[i].rows, params[i].cols);
-        auto it = std::find_if(buckets.begin(), buckets.end(), [&](const auto& b) { return b.first == key; });
-        if (it == buckets.end()) {
-            buckets.push_back({key, {i}});
-        } else {
-            it->second.push_back(i);
-        }
-    }
-    Coeffs cf;
-    RET(load_coeffs(nullptr, 5, cf));
-    for (auto& bk : buckets) {
-        const int R = bk.first.first, C = bk.first.second;
-        const int G = static_cast<int>(bk.second.size());
-        const BucketGeom g = make_geom(R, C);
-        const bool fused = muon_fused();
-        const int Gc = chunk_size(g, G, false, !fused);
-        const size_t meta_bytes = static_cast<size_t>(Gc) * (3 * sizeof(void*) + sizeof(long long)) + 256;
-        const Layout L = make_layout(g, Gc, false, !fused, meta_bytes);
-        RET(ensure_workspace(*st, L.total));
-        const long long numel = static_cast<long long>(R) * C;
-        const long long ld_o = round_up_ll(C, 8);
-        const float scale = 0.2f * std::sqrt(static_cast<float>(std::max(R, C)));
-        for (int g0 = 0; g0 < G; g0 += Gc) {
-            const int gc = std::min(Gc, G - g0);
-            std::vector<const void*> ptrs(3 * static_cast<size_t>(gc));
-            std::vector<long long> bases(gc);
-            for (int j = 0; j < gc; ++j) {
-                const int i = bk.second[g0 + j];
-                ptrs[j] = momentum[i].data;
-                ptrs[gc + j] = grads[i].data;
-                ptrs[2 * gc + j] = params[i].data;
-                bases[j] = params[i].base_index;
-            }
-            char* meta = st->ws + L.meta;
-            CK(cudaMemcpyAsync(meta, ptrs.data(), ptrs.size() * sizeof(void*), cudaMemcpyHostToDevice, s));
-            long long* bases_dev = reinterpret_cast<long long*>(meta + align_up(ptrs.size() * sizeof(void*), 16));
-            CK(cudaMemcpyAsync(bases_dev, bases.data(), bases.size() * sizeof(long long), cudaMemcpyHostToDevice, s));
-            const void* const* pm = reinterpret_cast<const void* const*>(meta);
-            MatrixSet Ms{nullptr, 0, pm};
-            MatrixSet Gs{nullptr, 0, pm + gc};
-            MatrixSet Ws{nullptr, 0, pm + 2 * gc};
-            OutSpec os;
-            os.out.rows = R;
-            os.out.cols = C;
-            os.out.f32 = false;
-            MuonFuse mf{};
-            if (fused) {
-                mf.w = reinterpret_cast<uint16_t* const*>(meta) + 2 * gc;
-                mf.base = bases_dev;
-                mf.lr = lr;
-                mf.wd = wd;
-                mf.scale = scale;
-                mf.seed_lo = static_cast<uint32_t>(seed);
-                mf.seed_hi = static_cast<uint32_t>(seed >> 32);
-                mf.step_lo = static_cast<uint32_t>(step);
-                mf.step_hi = static_cast<uint32_t>(step >> 32);
-                os.muon = &mf;
-            } else {
-                os.out.p = st->ws + L.o16;
-                os.out.ld = ld_o;
-                os.out.stride = static_cast<long long>(R) * ld_o;
-            }
-            RET(run_core(*st, g, L, gc, Ms, &Gs, mu, 5, 2, cf, os, s));
-            if (!fused) {
-                MatrixSet Os{os.out.p, os.out.stride, nullptr};
-                LAUNCH(kClsMuon,
-                       launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s));
-            }
-        }
-    }
-    return GNS_OK;
+    return optimizer_step(params, grads, momentum, nullptr, n, lr, wd, mu, 0.0f, 0.0f, seed, step, stream);
+}
+
+int normuon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum,
+                 const gns_tensor* second_moments, int n, float lr, float wd, float mu, float beta2, float eps,
+                 uint64_t seed, uint64_t step, void* stream) {
+    if (n > 0 && !second_moments) return fail(GNS_ERR_INVALID, "null second-moment array");
+    return optimizer_step(params, grads, momentum, second_moments, n, lr, wd, mu, beta2, eps, seed, step, stream);
 }
 
 int gns_muon_momentum(float* M, const uint16_t* G_bf16, int64_t numel, float mu, void* stream) {

@@ -450,11 +450,14 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(MatrixSet Ms, Matrix
                                  threadIdx.x);
 }
 
-// One thread per group of 4 global indices g = 4 blk .. 4 blk + 3.
+// One thread per group of 4 global indices g = 4 blk .. 4 blk + 3. With
+// row_step (NorMuon), row r of matrix g takes the step row_step[g R + r]
+// instead of lr * scale.
 __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, MatrixSet Os, long long ld_o,
                                                                const long long* base_dev, long long base_scalar,
                                                                int R, int C, float lr, float wd, float scale,
-                                                               uint32_t k0, uint32_t k1, uint32_t s0, uint32_t s1) {
+                                                               const float* row_step, uint32_t k0, uint32_t k1,
+                                                               uint32_t s0, uint32_t s1) {
     grid_dependency_wait();
     grid_launch_dependents();
     const int g = blockIdx.y;
@@ -463,7 +466,8 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
     const long long base = base_dev ? base_dev[g] : base_scalar;
     const long long numel = static_cast<long long>(R) * C;
     const float decay = __fsub_rn(1.0f, __fmul_rn(lr, wd));
-    const float stepv = __fmul_rn(lr, scale);
+    const float step_all = __fmul_rn(lr, scale);
+    const float* rs = row_step ? row_step + static_cast<long long>(g) * R : nullptr;
     // Blocks of the global index space that overlap [base, base + numel).
     const long long blk_first = base >> 2;
     const long long blk_last = (base + numel - 1) >> 2;
@@ -479,6 +483,7 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
         const long long i0 = blk * 4 - base;  // local index of global index 4 blk
         if (fast) {
             const long long r = i0 / C, col = i0 - r * C;
+            const float stepv = rs ? rs[r] : step_all;
             const uint2 wraw = *reinterpret_cast<const uint2*>(W + i0);
             const uint2 oraw = *reinterpret_cast<const uint2*>(O + r * ld_o + col);
             const uint16_t* wv = reinterpret_cast<const uint16_t*>(&wraw);
@@ -501,6 +506,7 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
                 const long long i = i0 + e;
                 if (i < 0 || i >= numel) continue;
                 const long long r = i / C, col = i - r * C;
+                const float stepv = rs ? rs[r] : step_all;
                 const float w = __uint_as_float(static_cast<uint32_t>(W[i]) << 16);
                 const float o = __half2float(O[r * ld_o + col]);
                 const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
@@ -508,6 +514,83 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
             }
         }
     }
+}
+
+// NorMuon (Dion3 Eq. 2), fp32 throughout. One warp per row r of matrix g:
+// s = sum_j O_rj^2 (lane l takes the 8-column groups l, l + 32, ... in
+// order, then a fixed butterfly), v_r <- beta2 v_r + (1 - beta2) s / C,
+// inv_r = 1 / (sqrt(v_r) + eps); stores s and s inv_r^2 for the norms.
+__global__ void __launch_bounds__(kThreads) normuon_rows_kernel(MatrixSet Os, long long ld_o, MatrixSet Vs, int R,
+                                                                int C, float beta2, float eps, float* row_sq,
+                                                                float* row_hat, float* inv) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int g = blockIdx.y;
+    const int r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= R) return;
+    const __half* o = mat_ptr<const __half>(Os, g) + static_cast<long long>(r) * ld_o;
+    float s = 0.0f;
+    const int groups = C / 8;
+    for (int q = lane; q < groups; q += 32) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(o + 8 * q);
+        const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(h[e]);
+            s = fmaf(f.x, f.x, s);
+            s = fmaf(f.y, f.y, s);
+        }
+    }
+    for (int j = 8 * groups + lane; j < C; j += 32) {
+        const float f = __half2float(o[j]);
+        s = fmaf(f, f, s);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) {
+        float* v = mat_ptr<float>(Vs, g) + r;
+        const float vn = __fadd_rn(__fmul_rn(beta2, *v), __fmul_rn(__fsub_rn(1.0f, beta2), __fdiv_rn(s, static_cast<float>(C))));
+        *v = vn;
+        const float iv = __frcp_rn(__fadd_rn(__fsqrt_rn(vn), eps));
+        const long long k = static_cast<long long>(g) * R + r;
+        row_sq[k] = s;
+        row_hat[k] = __fmul_rn(__fmul_rn(s, iv), iv);
+        inv[k] = iv;
+    }
+}
+
+// One block per matrix: ||O||^2 and ||O^||^2 summed over the rows in a fixed
+// order, factor = lr scale ||O|| / ||O^|| (0 when O^ = 0), and the per-row
+// steps row_step_r = factor inv_r.
+__global__ void __launch_bounds__(kThreads) normuon_factor_kernel(const float* row_sq, const float* row_hat,
+                                                                  const float* inv, int R, float lr_scale,
+                                                                  float* row_step) {
+    __shared__ float s_sq[kThreads], s_hat[kThreads];
+    __shared__ float s_factor;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const long long off = static_cast<long long>(blockIdx.x) * R;
+    float a = 0.0f, b = 0.0f;
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+        a += row_sq[off + r];
+        b += row_hat[off + r];
+    }
+    s_sq[threadIdx.x] = a;
+    s_hat[threadIdx.x] = b;
+    __syncthreads();
+    for (int w = kThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) {
+            s_sq[threadIdx.x] += s_sq[threadIdx.x + w];
+            s_hat[threadIdx.x] += s_hat[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        s_factor = s_hat[0] > 0.0f ? __fmul_rn(lr_scale, __fsqrt_rn(__fdiv_rn(s_sq[0], s_hat[0]))) : 0.0f;
+    __syncthreads();
+    const float f = s_factor;
+    for (int r = threadIdx.x; r < R; r += kThreads) row_step[off + r] = __fmul_rn(f, inv[off + r]);
 }
 
 int grid_for(long long work, int per_block_items) {
@@ -579,13 +662,28 @@ int launch_momentum(const MatrixSet& M, const MatrixSet& Gr, long long numel, in
     return launch_pdl(momentum_kernel, dim3(nblk, count), dim3(kThreads), s, M, Gr, numel, nblk, mu);
 }
 
+int launch_normuon_rows(const MatrixSet& O, long long ld_o, const MatrixSet& V, int count, int R, int C, float beta2,
+                        float eps, float* row_sq, float* row_hat, float* inv, cudaStream_t s) {
+    if (count <= 0 || R <= 0) return cudaSuccess;
+    const int rows_per_block = kThreads / 32;
+    return launch_pdl(normuon_rows_kernel, dim3((R + rows_per_block - 1) / rows_per_block, count), dim3(kThreads), s,
+                      O, ld_o, V, R, C, beta2, eps, row_sq, row_hat, inv);
+}
+
+int launch_normuon_factor(const float* row_sq, const float* row_hat, const float* inv, int count, int R,
+                          float lr_scale, float* row_step, cudaStream_t s) {
+    if (count <= 0 || R <= 0) return cudaSuccess;
+    return launch_pdl(normuon_factor_kernel, dim3(count), dim3(kThreads), s, row_sq, row_hat, inv, R, lr_scale,
+                      row_step);
+}
+
 int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o, const long long* base_dev,
                        long long base_scalar, int count, int R, int C, float lr, float wd, float scale,
-                       uint64_t seed, uint64_t step, cudaStream_t s) {
+                       uint64_t seed, uint64_t step, cudaStream_t s, const float* row_step) {
     if (count <= 0 || static_cast<long long>(R) * C <= 0) return cudaSuccess;
     const long long groups = static_cast<long long>(R) * C / 4 + 2;
     return launch_pdl(muon_update_kernel, dim3(grid_for(groups, kThreads * 4), count), dim3(kThreads), s, W, O,
-                      ld_o, base_dev, base_scalar, R, C, lr, wd, scale, static_cast<uint32_t>(seed),
+                      ld_o, base_dev, base_scalar, R, C, lr, wd, scale, row_step, static_cast<uint32_t>(seed),
                       static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(step),
                       static_cast<uint32_t>(step >> 32));
 }

@@ -64,10 +64,23 @@ int launch_momentum(const MatrixSet& M, const MatrixSet& Gr, long long numel, in
 
 // W[g] <- SR_bf16((1 - lr wd) W[g] - (lr scale) O[g]) with Philox keyed by
 // (seed, step, base + i), base = base_dev[g] when base_dev is not null, else
-// base_scalar. O[g] is fp16 R x C with row stride ld_o.
+// base_scalar. O[g] is fp16 R x C with row stride ld_o. With row_step
+// (NorMuon), row r of matrix g uses the step row_step[g R + r] in place of
+// lr scale.
 int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o,
                        const long long* base_dev, long long base_scalar, int count, int R, int C,
                        float lr, float wd, float scale, uint64_t seed, uint64_t step,
-                       cudaStream_t s);
+                       cudaStream_t s, const float* row_step = nullptr);
+
+// NorMuon statistics (Dion3 Eq. 2), fp32: per row r of O[g] (fp16 R x C,
+// row stride ld_o, a multiple of 8), v_r <- beta2 v_r + (1 - beta2) mean_j
+// O_rj^2 into V[g] (fp32 length R, in place), inv_r = 1 / (sqrt(v_r) + eps),
+// and row_sq / row_hat = sum_j O_rj^2 and its scaled counterpart
+// ([count][R] each). Then launch_normuon_factor turns them into the per-row
+// steps row_step = lr scale (||O|| / ||O^||) inv_r, [count][R].
+int launch_normuon_rows(const MatrixSet& O, long long ld_o, const MatrixSet& V, int count, int R, int C, float beta2,
+                        float eps, float* row_sq, float* row_hat, float* inv, cudaStream_t s);
+int launch_normuon_factor(const float* row_sq, const float* row_hat, const float* inv, int count, int R,
+                          float lr_scale, float* row_step, cudaStream_t s);
 
 }  // namespace gns

@@ -150,3 +150,68 @@ def test_fused_update_matches_separate_pass_bitwise(gns, monkeypatch):
     for i in range(len(shapes)):
         assert np.array_equal(m_sep[i], m_fused[i]), shapes[i]
         assert np.array_equal(w_sep[i], w_fused[i]), shapes[i]
+
+
+def _normuon_inputs(shapes, seed):
+    out = []
+    for i, (r, c) in enumerate(shapes):
+        w, g = gen.muon_param_inputs(r, c, seed=seed, index=i)
+        m = gen.gaussian(r, c, seed=seed + 1, index=i, scale=1e-3)
+        v = np.abs(gen.gaussian(r, 1, seed=seed + 2, index=i, scale=1e-4))[:, 0]  # a previous step's state
+        out.append((torch.from_numpy(w).to(torch.bfloat16), torch.from_numpy(g).to(torch.bfloat16),
+                    torch.from_numpy(m), torch.from_numpy(v.astype(np.float32))))
+    return out
+
+
+def test_normuon_step_matches_oracle(gns):
+    """NorMuon (Dion3 Eq. 2) against the oracle: momentum bitwise; the row
+    second moments and the update within the parity bar (they follow O)."""
+    shapes = [(128, 512), (512, 128), (96, 200), (256, 256), (128, 512)]
+    inputs = _normuon_inputs(shapes, 41)
+    bases = [0, 1 << 33, 1001, 5, 70000]
+    W = [w.cuda() for w, _, _, _ in inputs]
+    Gr = [g.cuda() for _, g, _, _ in inputs]
+    M = [m.cuda() for _, _, m, _ in inputs]
+    V = [v.cuda() for _, _, _, v in inputs]
+    gns.normuon_step(W, Gr, M, V, lr=0.02, wd=0.01, mu=0.95, beta2=0.95, eps=1e-8, seed=0, step=3,
+                     base_indices=bases)
+    torch.cuda.synchronize()
+    assert gns.gns_get_status() == 0
+    w_bits = [bf16_bits(w) for w, _, _, _ in inputs]
+    new_w, new_m, new_v, dirs = MU.normuon_step(w_bits, [bf16_bits(g) for _, g, _, _ in inputs],
+                                                [m.numpy() for _, _, m, _ in inputs],
+                                                [v.numpy().astype(np.float64) for _, _, _, v in inputs],
+                                                0.02, 0.01, 0.95, 0.95, 1e-8, 0, 3, bases)
+    for i, (r, c) in enumerate(shapes):
+        assert np.array_equal(M[i].cpu().numpy(), new_m[i]), f"momentum {i}"
+        v_got = V[i].cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(v_got - new_v[i]) <= 6e-2 * np.linalg.norm(new_v[i]), (i, "second moment")
+        w_old = MU.bf16_bits_to_f32(w_bits[i]).astype(np.float64)
+        got_delta = MU.bf16_bits_to_f32(bf16_bits(W[i])).astype(np.float64) - w_old
+        want_delta = MU.bf16_bits_to_f32(new_w[i]).astype(np.float64) - w_old
+        noise = np.linalg.norm(np.abs(w_old) * 2.0 ** -7) * 2
+        rel = np.linalg.norm(got_delta - want_delta) / np.linalg.norm(want_delta)
+        assert rel <= 3e-2 + noise / np.linalg.norm(want_delta), (i, rel)
+
+
+def test_normuon_grouped_equals_single_bitwise(gns):
+    shapes = [(192, 320)] * 3
+    inputs = _normuon_inputs(shapes, 51)
+
+    def run(groups):
+        W = [w.cuda() for w, _, _, _ in inputs]
+        Gr = [g.cuda() for _, g, _, _ in inputs]
+        M = [m.cuda() for _, _, m, _ in inputs]
+        V = [v.cuda() for _, _, _, v in inputs]
+        bases = [i * 192 * 320 for i in range(3)]
+        for idx in groups:
+            gns.normuon_step([W[i] for i in idx], [Gr[i] for i in idx], [M[i] for i in idx], [V[i] for i in idx],
+                             lr=0.02, wd=0.01, mu=0.95, seed=9, step=4, base_indices=[bases[i] for i in idx])
+        torch.cuda.synchronize()
+        assert gns.gns_get_status() == 0
+        return [bf16_bits(w) for w in W], [v.cpu().numpy() for v in V]
+
+    w_all, v_all = run([[0, 1, 2]])
+    w_one, v_one = run([[0], [1], [2]])
+    for i in range(3):
+        assert np.array_equal(w_all[i], w_one[i]) and np.array_equal(v_all[i], v_one[i]), i
