@@ -138,3 +138,52 @@ def test_normuon_mutant_is_caught(name):
     old, new = NORMUON_MUTANTS[name]
     assert src.count(old) == 1, f"mutation site not unique/found: {name}"
     assert not normuon_pins_pass(load_variant(f"muon_{name}", src.replace(old, new)))
+
+
+# Dion3 update rule (Algorithm 4) in oracle/dion3.py.
+D3_SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "dion3.py")
+
+DION3_MUTANTS = {
+    "dion3_smallest_rows": ("order = np.lexsort((np.arange(n), -l1))", "order = np.lexsort((np.arange(n), l1))"),
+    "dion3_l2_selection": ("l1 = np.abs(M).sum(axis=1)", "l1 = (M * M).sum(axis=1)"),
+    "dion3_damp_every_row": ("        M_new[S] = np.float32(mu) * M_new[S]", "        M_new = np.float32(mu) * M_new"),
+    "dion3_momentum_damped_first": ("M = MU.momentum(M, MU.bf16_bits_to_f32(g_bits), 1.0)",
+                                    "M = MU.momentum(M, MU.bf16_bits_to_f32(g_bits), mu)"),
+    "dion3_rows_always": ("cols = R > C", "cols = False"),
+    "dion3_floor_count": ("int(math.ceil(f * n - 1e-9))", "int(math.floor(f * n))"),
+}
+
+
+def dion3_pins_pass(D3):
+    import tests.test_oracle_dion3 as T
+    saved = T.D3
+    T.D3 = D3
+    try:
+        for name in dir(T):
+            if name.startswith("test_"):
+                getattr(T, name)()
+    except Exception:
+        return False
+    finally:
+        T.D3 = saved
+    return True
+
+
+def load_oracle_module(name, source):
+    spec = importlib.util.spec_from_loader(f"oracle.{name}", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    exec(compile(source, name, "exec"), mod.__dict__)
+    return mod
+
+
+def test_dion3_original_passes():
+    assert dion3_pins_pass(load_oracle_module("dion3_original", open(D3_SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(DION3_MUTANTS))
+def test_dion3_mutant_is_caught(name):
+    src = open(D3_SRC).read()
+    old, new = DION3_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site not unique/found: {name}"
+    assert not dion3_pins_pass(load_oracle_module(f"dion3_{name}", src.replace(old, new)))
