@@ -18,7 +18,7 @@ def test_selection_count_and_order():
     assert list(D3.select(M, 0.4)) == [1, 3]
     # The l1 norm, not the l2 norm: a spread row beats a peaked one.
     P = np.array([[3.0, 0.0, 0.0, 0.0], [1.0, 1.0, 1.0, 1.0], [0.1, 0.0, 0.0, 0.0]])
-    assert list(D3.select(P, 0.34)) == [1]
+    assert list(D3.select(P, 0.3)) == [1]
 
 
 def _inputs(R, C, seed):
