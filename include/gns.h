@@ -159,6 +159,22 @@ int normuon_step(const gns_tensor* params, const gns_tensor* grads, const gns_te
                  float eps, uint64_t seed, uint64_t step, void* stream);
 
 /*
+ * dion3_step: one step of the Dion3 update rule (Dion3 §6, Algorithm 4,
+ * Muon flavor) over n weight matrices:
+ *   M <- M + G                                        (fp32)
+ *   S <- the k = ceil(fraction * d) rows of M with the largest l1 norm, d the
+ *        row count, or the columns when they are fewer (d = cols); largest
+ *        first, equal norms by lower index
+ *   O <- gns(M[S])                                    (k x max(rows, cols))
+ *   W <- SR_bf16((1 - lr*wd) W - lr*s*O~),  O~ = O on S and 0 elsewhere,
+ *        s = 0.2 sqrt(max(rows, cols)), stochastic rounding as muon_step
+ *   M[S] <- mu M[S]                                   (error feedback)
+ * fraction in (0, 1]; min(rows, cols) <= 16384. Other arguments as muon_step.
+ */
+int dion3_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n,
+               float fraction, float lr, float wd, float mu, uint64_t seed, uint64_t step, void* stream);
+
+/*
  * gns_muon_momentum: the first elementwise pass of muon_step on one tensor:
  * M <- mu*M + float(G), fp32, two roundings (Dion3 Eq. 1).
  *   M      device fp32 [numel], updated in place.

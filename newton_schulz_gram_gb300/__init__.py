@@ -14,7 +14,7 @@ import torch
 from ._lib import GnsError, GnsTensor, check, load
 
 __all__ = ["gns_orthogonalize_batched", "gns_orthogonalize_batched_host",
-           "gns_orthogonalize_batched_noalloc", "muon_step", "normuon_step",
+           "gns_orthogonalize_batched_noalloc", "muon_step", "normuon_step", "dion3_step",
            "gns_muon_momentum", "gns_muon_update", "gns_symm_gemm", "gns_get_status",
            "gns_status_string", "gns_last_error", "gns_workspace_bytes", "gns_release",
            "gns_launch_count", "gns_profile_enable", "gns_profile_read", "KERNEL_CLASSES",
@@ -122,6 +122,27 @@ def muon_step(params, grads, momenta, lr, wd, mu, seed, step, base_indices=None,
     M = _tensors(momenta, torch.float32, "momenta")
     lib = load()
     check(lib.muon_step(P, Gr, M, n, lr, wd, mu, seed, step, _stream(stream, params[0].device)), "muon_step")
+
+
+def dion3_step(params, grads, momenta, fraction, lr, wd, mu, seed=0, step=0, base_indices=None, stream=None):
+    """One Dion3 step (Algorithm 4, Muon flavor) over lists of bf16 params (in
+    place), bf16 grads and fp32 momenta (in place)."""
+    n = len(params)
+    if len(grads) != n or len(momenta) != n:
+        raise ValueError("params, grads and momenta must have equal lengths")
+    if n == 0:
+        return
+    if base_indices is None:
+        base_indices, acc = [], 0
+        for p in params:
+            base_indices.append(acc)
+            acc += p.numel()
+    P = _tensors(params, torch.bfloat16, "params", base_indices)
+    Gr = _tensors(grads, torch.bfloat16, "grads")
+    M = _tensors(momenta, torch.float32, "momenta")
+    lib = load()
+    check(lib.dion3_step(P, Gr, M, n, fraction, lr, wd, mu, seed, step, _stream(stream, params[0].device)),
+          "dion3_step")
 
 
 def normuon_step(params, grads, momenta, second_moments, lr, wd, mu, beta2=0.95, eps=1e-8, seed=0, step=0,

@@ -28,6 +28,8 @@ PROTOTYPES = {
     "gns_orthogonalize_batched_noalloc": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "muon_step": (_i, [ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor),
                        _i, _f, _f, _f, _u64, _u64, _vp]),
+    "dion3_step": (_i, [ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor),
+                        _i, _f, _f, _f, _f, _u64, _u64, _vp]),
     "normuon_step": (_i, [ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor),
                           ctypes.POINTER(GnsTensor), _i, _f, _f, _f, _f, _f, _u64, _u64, _vp]),
     "gns_muon_momentum": (_i, [_vp, _vp, _i64, _f, _vp]),

@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build", platform.machine())
 LIB = os.path.join(BUILD, "libgns.so")
-SOURCES = ["gemm_tc.cu", "elementwise.cu", "api.cu"]
+SOURCES = ["gemm_tc.cu", "elementwise.cu", "dion3.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -30,6 +30,7 @@
 #include <string>
 #include <vector>
 
+#include "dion3.cuh"
 #include "elementwise.cuh"
 #include "gemm.cuh"
 #include "gns.h"
@@ -953,6 +954,107 @@ int optimizer_step(const gns_tensor* params, const gns_tensor* grads, const gns_
     return GNS_OK;
 }
 
+
+// One Dion3 step (Algorithm 4, Muon flavor) over n matrices, bucketed by
+// shape: accumulate and rank, gather the selected rows (or columns), run the
+// Gram NS core on the k x m submatrices, then update W and damp M.
+int dion3_step_impl(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n,
+                    float fraction, float lr, float wd, float mu, uint64_t seed, uint64_t step, void* stream) {
+    if (n < 0) return fail(GNS_ERR_INVALID, "n < 0");
+    if (n == 0) return GNS_OK;
+    if (!params || !grads || !momentum) return fail(GNS_ERR_INVALID, "null tensor array");
+    if (!(fraction > 0.0f && fraction <= 1.0f)) return fail(GNS_ERR_INVALID, "fraction must be in (0, 1]");
+    for (int i = 0; i < n; ++i) {
+        const gns_tensor &w = params[i], &gr = grads[i], &mm = momentum[i];
+        if (!w.data || !gr.data || !mm.data) return fail(GNS_ERR_INVALID, "null tensor data");
+        if (w.rows < 1 || w.cols < 1 || gr.rows != w.rows || gr.cols != w.cols || mm.rows != w.rows ||
+            mm.cols != w.cols)
+            return fail(GNS_ERR_INVALID, "tensor shapes differ");
+        if (w.base_index < 0) return fail(GNS_ERR_INVALID, "negative base_index");
+        if (std::min(w.rows, w.cols) > kDion3MaxSelect)
+            return fail(GNS_ERR_UNSUPPORTED, "selection dimension above " + std::to_string(kDion3MaxSelect));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    std::vector<std::pair<std::pair<int, int>, std::vector<int>>> buckets;
+    for (int i = 0; i < n; ++i) {
+        auto key = std::make_pair(params[i].rows, params[i].cols);
+        auto it = std::find_if(buckets.begin(), buckets.end(), [&](const auto& b) { return b.first == key; });
+        if (it == buckets.end()) {
+            buckets.push_back({key, {i}});
+        } else {
+            it->second.push_back(i);
+        }
+    }
+    Coeffs cf;
+    RET(load_coeffs(nullptr, 5, cf));
+    for (auto& bk : buckets) {
+        const int R = bk.first.first, C = bk.first.second;
+        const int G = static_cast<int>(bk.second.size());
+        const bool cols = R > C;  // select along the smaller dimension
+        const int nsel = cols ? C : R, m = cols ? R : C;
+        const int k = dion3_selection_count(nsel, fraction);
+        const BucketGeom g = make_geom(k, m);
+        const float scale = 0.2f * std::sqrt(static_cast<float>(std::max(R, C)));
+        // Per matrix: 3 pointers, a base, the norms, the selection, the
+        // positions and the gathered fp32 submatrix, all in the metadata block.
+        const size_t per_meta = 3 * sizeof(void*) + sizeof(long long) + 8 * static_cast<size_t>(nsel) +
+                                4 * static_cast<size_t>(k) + 4 * static_cast<size_t>(k) * m + 1024;
+        int Gc = std::min(G, 65535);
+        while (Gc > 1 && make_layout(g, Gc, false, true, static_cast<size_t>(Gc) * per_meta).total > chunk_cap_bytes())
+            Gc = (Gc + 1) / 2;
+        const Layout L = make_layout(g, Gc, false, true, static_cast<size_t>(Gc) * per_meta);
+        RET(ensure_workspace(*st, L.total));
+        const long long ld_o = round_up_ll(m, 8);
+        for (int g0 = 0; g0 < G; g0 += Gc) {
+            const int gc = std::min(Gc, G - g0);
+            std::vector<const void*> ptrs(3 * static_cast<size_t>(gc));
+            std::vector<long long> bases(gc);
+            for (int j = 0; j < gc; ++j) {
+                const int i = bk.second[g0 + j];
+                ptrs[j] = momentum[i].data;
+                ptrs[gc + j] = grads[i].data;
+                ptrs[2 * gc + j] = params[i].data;
+                bases[j] = params[i].base_index;
+            }
+            char* meta = st->ws + L.meta;
+            size_t off = 0;
+            auto carve = [&](size_t bytes) {
+                char* p = meta + off;
+                off = align_up(off + bytes, 256);
+                return p;
+            };
+            char* ptr_block = carve(ptrs.size() * sizeof(void*));
+            long long* bases_dev = reinterpret_cast<long long*>(carve(bases.size() * sizeof(long long)));
+            float* l1 = reinterpret_cast<float*>(carve(sizeof(float) * static_cast<size_t>(gc) * nsel));
+            int* sel = reinterpret_cast<int*>(carve(sizeof(int) * static_cast<size_t>(gc) * k));
+            int* pos = reinterpret_cast<int*>(carve(sizeof(int) * static_cast<size_t>(gc) * nsel));
+            float* X = reinterpret_cast<float*>(carve(sizeof(float) * static_cast<size_t>(gc) * k * m));
+            CK(cudaMemcpyAsync(ptr_block, ptrs.data(), ptrs.size() * sizeof(void*), cudaMemcpyHostToDevice, s));
+            CK(cudaMemcpyAsync(bases_dev, bases.data(), bases.size() * sizeof(long long), cudaMemcpyHostToDevice, s));
+            const void* const* pm = reinterpret_cast<const void* const*>(ptr_block);
+            MatrixSet Ms{nullptr, 0, pm};
+            MatrixSet Gs{nullptr, 0, pm + gc};
+            MatrixSet Ws{nullptr, 0, pm + 2 * gc};
+            LAUNCH(kClsMuon, launch_dion3_accumulate(Ms, Gs, gc, R, C, cols, l1, s));
+            LAUNCH(kClsMuon, launch_dion3_select(l1, gc, nsel, k, sel, pos, s));
+            LAUNCH(kClsMuon, launch_dion3_gather(Ms, gc, R, C, cols, sel, k, X, s));
+            OutSpec os;
+            os.out.p = st->ws + L.o16;
+            os.out.rows = k;
+            os.out.cols = m;
+            os.out.ld = ld_o;
+            os.out.stride = static_cast<long long>(k) * ld_o;
+            os.out.f32 = false;
+            const MatrixSet Xs{X, static_cast<long long>(k) * m, nullptr};
+            RET(run_core(*st, g, L, gc, Xs, nullptr, 0.0f, 5, 2, cf, os, s));
+            LAUNCH(kClsMuon, launch_dion3_update(Ws, Ms, os.out.p, ld_o, os.out.stride, pos, nsel, bases_dev, gc, R, C,
+                                                 cols, lr, wd, scale, mu, seed, step, s));
+        }
+    }
+    return GNS_OK;
+}
 }  // namespace
 }  // namespace gns
 
@@ -997,6 +1099,11 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
 int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n, float lr,
               float wd, float mu, uint64_t seed, uint64_t step, void* stream) {
     return optimizer_step(params, grads, momentum, nullptr, n, lr, wd, mu, 0.0f, 0.0f, seed, step, stream);
+}
+
+int dion3_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n,
+               float fraction, float lr, float wd, float mu, uint64_t seed, uint64_t step, void* stream) {
+    return dion3_step_impl(params, grads, momentum, n, fraction, lr, wd, mu, seed, step, stream);
 }
 
 int normuon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum,
