@@ -73,6 +73,17 @@ int gns_orthogonalize_batched(float* ptr, int G, int R, int C, int steps, int re
                               const float* coeffs, void* stream);
 
 /*
+ * gns_orthogonalize_batched_schedule: gns_orthogonalize_batched with any
+ * restart schedule (Dion3 App. B.2.1 chooses one per coefficient schedule):
+ * bit t of restart_mask set (1 <= t < steps) = restart after step t
+ * (X <- Q X, R <- X X^T, Q <- I). Other bits set: GNS_ERR_INVALID. The
+ * periodic restart_at of gns_orthogonalize_batched is the mask with the
+ * multiples t of restart_at that leave at least restart_at steps.
+ */
+int gns_orthogonalize_batched_schedule(float* ptr, int G, int R, int C, int steps, uint64_t restart_mask,
+                                       const float* coeffs, void* stream);
+
+/*
  * gns_orthogonalize_batched_host: the same computation on a HOST buffer.
  * host_ptr is fp32 [G][R][C] in host memory (pinned memory gives full copy
  * speed); the library copies it to a device staging buffer it owns, runs

@@ -14,7 +14,7 @@ import torch
 from ._lib import GnsError, GnsTensor, check, load
 
 __all__ = ["gns_orthogonalize_batched", "gns_orthogonalize_batched_host",
-           "gns_orthogonalize_batched_noalloc", "muon_step", "normuon_step", "dion3_step",
+           "gns_orthogonalize_batched_noalloc", "gns_orthogonalize_batched_schedule", "muon_step", "normuon_step", "dion3_step",
            "gns_muon_momentum", "gns_muon_update", "gns_symm_gemm", "gns_get_status",
            "gns_status_string", "gns_last_error", "gns_workspace_bytes", "gns_release",
            "gns_launch_count", "gns_profile_enable", "gns_profile_read", "KERNEL_CLASSES",
@@ -60,6 +60,22 @@ def gns_orthogonalize_batched(x, steps=5, restart_at=2, coeffs=None, stream=None
     lib = load()
     check(lib.gns_orthogonalize_batched(ctypes.c_void_p(x.data_ptr()), G, R, C, steps, restart_at,
                                         cptr, _stream(stream, x.device)), "gns_orthogonalize_batched")
+    del keep
+    return x
+
+
+def gns_orthogonalize_batched_schedule(x, steps=5, restarts=(2,), coeffs=None, stream=None):
+    """Orthogonalize x in place with an explicit restart schedule: restart
+    after each step t in `restarts` (1 <= t < steps); see restart_schedule."""
+    _require(x, torch.float32, name="x")
+    G, R, C = (1, *x.shape) if x.dim() == 2 else tuple(x.shape)
+    keep, cptr = _coeff_array(coeffs, steps)
+    mask = 0
+    for t in restarts:
+        mask |= 1 << int(t)
+    lib = load()
+    check(lib.gns_orthogonalize_batched_schedule(ctypes.c_void_p(x.data_ptr()), G, R, C, steps, mask, cptr,
+                                                 _stream(stream, x.device)), "gns_orthogonalize_batched_schedule")
     del keep
     return x
 

@@ -24,6 +24,7 @@ class GnsTensor(ctypes.Structure):
 
 PROTOTYPES = {
     "gns_orthogonalize_batched": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "gns_orthogonalize_batched_schedule": (_i, [_vp, _i, _i, _i, _i, _u64, _vp, _vp]),
     "gns_orthogonalize_batched_host": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "gns_orthogonalize_batched_noalloc": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "muon_step": (_i, [ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor),

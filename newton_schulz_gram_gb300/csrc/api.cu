@@ -462,8 +462,20 @@ int load_coeffs(const float* coeffs, int steps, Coeffs& out) {
     return GNS_OK;
 }
 
-bool is_restart_after(int t, int steps, int restart_at) {
-    return restart_at > 0 && t >= 1 && t < steps && t % restart_at == 0 && steps - t >= restart_at;
+// Restart schedules as bit masks: bit t set = restart after step t
+// (1 <= t < steps). The periodic schedule restarts after every multiple of
+// restart_at that leaves at least one full period (Dion3 Algorithm 3: T = 5,
+// restart_at = 2 restarts once, after step 2).
+uint64_t periodic_restarts(int steps, int restart_at) {
+    uint64_t m = 0;
+    if (restart_at <= 0) return 0;
+    for (int t = 1; t < steps; ++t)
+        if (t % restart_at == 0 && steps - t >= restart_at) m |= uint64_t(1) << t;
+    return m;
+}
+
+bool is_restart_after(int t, int steps, uint64_t restarts) {
+    return t >= 1 && t < steps && ((restarts >> t) & 1);
 }
 
 // Where the result of one bucket goes.
@@ -549,7 +561,7 @@ Mat mat16(char* ws, size_t off, int rows, int cols, long long ld) {
 // Runs the orthogonalization of one chunk of Gc fp32 matrices `in` (the
 // momentum, first updated in place as M <- mu M + G, when grads is given).
 int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in,
-             const MatrixSet* grads, float mu, int steps, int restart_at, const Coeffs& cf, const OutSpec& os,
+             const MatrixSet* grads, float mu, int steps, uint64_t restarts, const Coeffs& cf, const OutSpec& os,
              cudaStream_t s) {
     const TileShape ts = choose_tile(g.n);
     ProgramBuilder prog(st, Gc, ts, reinterpret_cast<int*>(st.ws + L.counters), s);
@@ -675,7 +687,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     bool q_identity = true;
     for (int t = 1; t <= steps; ++t) {
         const float a = cf.a[t - 1], b = cf.b[t - 1], c = cf.c[t - 1];
-        if (is_restart_after(t - 1, steps, restart_at)) {
+        if (is_restart_after(t - 1, steps, restarts)) {
             // X <- Q X, then R <- X X^T, Q <- I.
             ProblemSpec p;
             qx(p);
@@ -685,7 +697,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             RET(gram());
             q_identity = true;
         }
-        const bool need_r = t < steps && !is_restart_after(t, steps, restart_at);
+        const bool need_r = t < steps && !is_restart_after(t, steps, restarts);
         // Z = b R + c R^2 (with Q = Z + a I written alongside after a (re)start).
         {
             ProblemSpec p;
@@ -786,7 +798,7 @@ int chunk_size(const BucketGeom& g, int G, bool out32, bool o16) {
     return static_cast<int>(c);
 }
 
-int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart_at, const float* coeffs,
+int orthogonalize_device(float* ptr, int G, int R, int C, int steps, uint64_t restarts, const float* coeffs,
                          cudaStream_t s) {
     RET(validate_common(G, R, C, steps));
     if (G == 0) return GNS_OK;
@@ -821,7 +833,7 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, int restart
             os.out.stride = static_cast<long long>(R) * L.ld_out32;
             os.out.f32 = true;
         }
-        RET(run_core(*st, g, L, gc, in, nullptr, 0.0f, steps, restart_at, cf, os, s));
+        RET(run_core(*st, g, L, gc, in, nullptr, 0.0f, steps, restarts, cf, os, s));
         if (!direct_out)
             LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
     }
@@ -931,7 +943,7 @@ int optimizer_step(const gns_tensor* params, const gns_tensor* grads, const gns_
                 os.out.ld = ld_o;
                 os.out.stride = static_cast<long long>(R) * ld_o;
             }
-            RET(run_core(*st, g, L, gc, Ms, &Gs, mu, 5, 2, cf, os, s));
+            RET(run_core(*st, g, L, gc, Ms, &Gs, mu, 5, periodic_restarts(5, 2), cf, os, s));
             if (fused) continue;
             MatrixSet Os{os.out.p, os.out.stride, nullptr};
             const float* row_step = nullptr;
@@ -1048,7 +1060,7 @@ int dion3_step_impl(const gns_tensor* params, const gns_tensor* grads, const gns
             os.out.stride = static_cast<long long>(k) * ld_o;
             os.out.f32 = false;
             const MatrixSet Xs{X, static_cast<long long>(k) * m, nullptr};
-            RET(run_core(*st, g, L, gc, Xs, nullptr, 0.0f, 5, 2, cf, os, s));
+            RET(run_core(*st, g, L, gc, Xs, nullptr, 0.0f, 5, periodic_restarts(5, 2), cf, os, s));
             LAUNCH(kClsMuon, launch_dion3_update(Ws, Ms, os.out.p, ld_o, os.out.stride, pos, nsel, bases_dev, gc, R, C,
                                                  cols, lr, wd, scale, mu, seed, step, s));
         }
@@ -1064,7 +1076,17 @@ extern "C" {
 
 int gns_orthogonalize_batched(float* ptr, int G, int R, int C, int steps, int restart_at, const float* coeffs,
                               void* stream) {
-    return orthogonalize_device(ptr, G, R, C, steps, restart_at, coeffs, static_cast<cudaStream_t>(stream));
+    if (steps < 1 || steps > GNS_MAX_STEPS) return fail(GNS_ERR_INVALID, "steps must be in 1..GNS_MAX_STEPS");
+    return orthogonalize_device(ptr, G, R, C, steps, periodic_restarts(steps, restart_at), coeffs,
+                                static_cast<cudaStream_t>(stream));
+}
+
+int gns_orthogonalize_batched_schedule(float* ptr, int G, int R, int C, int steps, uint64_t restart_mask,
+                                       const float* coeffs, void* stream) {
+    if (steps < 1 || steps > GNS_MAX_STEPS) return fail(GNS_ERR_INVALID, "steps must be in 1..GNS_MAX_STEPS");
+    const uint64_t valid = (steps >= 64 ? ~uint64_t(0) : ((uint64_t(1) << steps) - 1)) & ~uint64_t(1);
+    if (restart_mask & ~valid) return fail(GNS_ERR_INVALID, "restart mask bits must lie in 1..steps-1");
+    return orthogonalize_device(ptr, G, R, C, steps, restart_mask, coeffs, static_cast<cudaStream_t>(stream));
 }
 
 int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int steps, int restart_at,
@@ -1090,7 +1112,8 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
         st->stage_bytes = bytes;
     }
     CK(cudaMemcpyAsync(st->stage, host_ptr, bytes, cudaMemcpyHostToDevice, s));
-    RET(orthogonalize_device(st->stage, G, R, C, steps, restart_at, coeffs, s));
+    if (steps < 1 || steps > GNS_MAX_STEPS) return fail(GNS_ERR_INVALID, "steps must be in 1..GNS_MAX_STEPS");
+    RET(orthogonalize_device(st->stage, G, R, C, steps, periodic_restarts(steps, restart_at), coeffs, s));
     CK(cudaMemcpyAsync(host_ptr, st->stage, bytes, cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));
     return GNS_OK;
@@ -1366,7 +1389,7 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
             os.out.ld = L.ld_out32;
             os.out.stride = static_cast<long long>(R) * L.ld_out32;
         }
-        RET(run_core(st, g, L, gc, in, nullptr, 0.0f, steps, restart_at, cf, os, s));
+        RET(run_core(st, g, L, gc, in, nullptr, 0.0f, steps, periodic_restarts(steps, restart_at), cf, os, s));
         if (!direct_out)
             LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
     }

@@ -68,7 +68,11 @@ def coeff_schedule(steps, coeffs=None):
 
 
 def restart_points(steps, restart_at):
-    """Steps t (1-based) after which the Gram iteration restarts."""
+    """Steps t (1-based) after which the Gram iteration restarts: every
+    multiple of the period restart_at with at least one period left, or an
+    explicit list of steps (any schedule, Dion3 App. B.2.1 sweeps them)."""
+    if isinstance(restart_at, (list, tuple, set, frozenset)):
+        return sorted(t for t in set(restart_at) if 1 <= t < steps)
     if restart_at is None or restart_at <= 0:
         return []
     return [t for t in range(1, steps) if t % restart_at == 0 and steps - t >= restart_at]

@@ -144,3 +144,25 @@ def test_invalid_arguments_raise(gns):
         gns.gns_orthogonalize_batched(t, steps=0)
     with pytest.raises(ValueError):
         gns.gns_orthogonalize_batched(t, steps=2, coeffs=[1.0, 2.0])
+
+
+def test_restart_schedule_entry_point(gns):
+    """Any restart schedule (Dion3 App. B.2.1): the periodic one equals the
+    default entry point bit for bit; others match the oracle run with the
+    same restart steps; mask bits outside 1 .. steps - 1 are rejected."""
+    X = gen.gaussian_bucket(3, 256, 1024, seed=13)
+    ref = run_gpu(gns, X)
+    t = torch.from_numpy(X.copy()).cuda()
+    gns.gns_orthogonalize_batched_schedule(t, 5, (2,))
+    torch.cuda.synchronize()
+    assert np.array_equal(t.cpu().numpy(), ref)
+    for restarts in [(3,), (1,), (2, 3), ()]:
+        t = torch.from_numpy(X.copy()).cuda()
+        gns.gns_orthogonalize_batched_schedule(t, 5, restarts)
+        torch.cuda.synchronize()
+        assert gns.gns_get_status() == 0
+        out = t.cpu().numpy()
+        for g in range(3):
+            assert_parity(out[g], O.gram_ns(X[g].astype(np.float64), 5, None, list(restarts)), what=str(restarts))
+    with pytest.raises(Exception):
+        gns.gns_orthogonalize_batched_schedule(torch.from_numpy(X.copy()).cuda(), 5, (5,))
