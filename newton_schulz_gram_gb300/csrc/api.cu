@@ -75,6 +75,7 @@ struct DeviceState {
     int* err = nullptr;
     float* stage = nullptr;  // device staging for the host-buffer entry point
     size_t stage_bytes = 0;
+    cudaStream_t h2d = nullptr, d2h = nullptr;  // copy streams of the host-buffer entry point
 };
 
 std::mutex g_mu;
@@ -1111,12 +1112,63 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
         }
         st->stage_bytes = bytes;
     }
-    CK(cudaMemcpyAsync(st->stage, host_ptr, bytes, cudaMemcpyHostToDevice, s));
     if (steps < 1 || steps > GNS_MAX_STEPS) return fail(GNS_ERR_INVALID, "steps must be in 1..GNS_MAX_STEPS");
-    RET(orthogonalize_device(st->stage, G, R, C, steps, periodic_restarts(steps, restart_at), coeffs, s));
-    CK(cudaMemcpyAsync(host_ptr, st->stage, bytes, cudaMemcpyDeviceToHost, s));
-    CK(cudaStreamSynchronize(s));
-    return GNS_OK;
+    if (!st->h2d) CK(cudaStreamCreateWithFlags(&st->h2d, cudaStreamNonBlocking));
+    if (!st->d2h) CK(cudaStreamCreateWithFlags(&st->d2h, cudaStreamNonBlocking));
+    // Pipelined in chunks of about 64 MiB: chunk c's host-to-device copy (one
+    // copy stream), its orthogonalization (the caller's stream) and its
+    // device-to-host copy (the other copy stream) overlap with the
+    // neighbouring chunks' stages; events order the three stages of a chunk.
+    const long long per = static_cast<long long>(R) * C;
+    long long chunk_bytes = 64LL << 20;
+    if (const char* e = std::getenv("GNS_HOST_CHUNK_MB")) {
+        if (std::atoll(e) > 0) chunk_bytes = std::atoll(e) << 20;
+    }
+    const int gc = static_cast<int>(std::max(1LL, std::min<long long>(G, chunk_bytes / (per * 4))));
+    const int nchunks = (G + gc - 1) / gc;
+    std::vector<cudaEvent_t> ev(2 * static_cast<size_t>(nchunks) + 1, nullptr);
+    int rc = GNS_OK;
+    auto cleanup = [&]() {
+        for (cudaEvent_t e : ev)
+            if (e) cudaEventDestroy(e);
+    };
+    for (cudaEvent_t& e : ev) {
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            cleanup();
+            return fail(GNS_ERR_CUDA, "event creation failed");
+        }
+    }
+    const uint64_t restarts = periodic_restarts(steps, restart_at);
+    auto run = [&]() -> int {
+        // The copies start after the caller's earlier work on its stream.
+        CK(cudaEventRecord(ev[0], s));
+        CK(cudaStreamWaitEvent(st->h2d, ev[0], 0));
+        for (int c = 0; c < nchunks; ++c) {
+            const int g0 = c * gc, n = std::min(gc, G - g0);
+            float* dev = st->stage + static_cast<long long>(g0) * per;
+            float* host = host_ptr + static_cast<long long>(g0) * per;
+            const size_t b = static_cast<size_t>(n) * per * sizeof(float);
+            CK(cudaMemcpyAsync(dev, host, b, cudaMemcpyHostToDevice, st->h2d));
+            CK(cudaEventRecord(ev[1 + 2 * c], st->h2d));
+            CK(cudaStreamWaitEvent(s, ev[1 + 2 * c], 0));
+            RET(orthogonalize_device(dev, n, R, C, steps, restarts, coeffs, s));
+            CK(cudaEventRecord(ev[2 + 2 * c], s));
+            CK(cudaStreamWaitEvent(st->d2h, ev[2 + 2 * c], 0));
+            CK(cudaMemcpyAsync(host, dev, b, cudaMemcpyDeviceToHost, st->d2h));
+        }
+        CK(cudaStreamSynchronize(st->d2h));
+        CK(cudaStreamSynchronize(s));
+        return GNS_OK;
+    };
+    rc = run();
+    if (rc != GNS_OK) {
+        cudaStreamSynchronize(st->h2d);
+        cudaStreamSynchronize(st->d2h);
+        cudaStreamSynchronize(s);
+    }
+    cleanup();
+    return rc;
 }
 
 int muon_step(const gns_tensor* params, const gns_tensor* grads, const gns_tensor* momentum, int n, float lr,
@@ -1282,6 +1334,9 @@ void gns_release(void) {
     it->second.ws_bytes = 0;
     it->second.stage = nullptr;
     it->second.stage_bytes = 0;
+    if (it->second.h2d) cudaStreamDestroy(it->second.h2d);
+    if (it->second.d2h) cudaStreamDestroy(it->second.d2h);
+    it->second.h2d = it->second.d2h = nullptr;
 }
 
 }  // extern "C"
