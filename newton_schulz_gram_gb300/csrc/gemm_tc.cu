@@ -240,35 +240,55 @@ __device__ __forceinline__ void muon_update_row(const GemmProblem& pr, int g, in
         const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
         return sr_bf16(wn, u & 0xFFFFu);
     };
+    // Register arrays only: every index below is a compile-time constant
+    // (a runtime index would move v to local memory for every tile).
     if (ncol == 32 && (g0 & 3) == 0 && (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
-        uint4 wv[4];
+        uint32_t wv[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) wv[k] = reinterpret_cast<const uint4*>(wp)[k];
-        uint16_t* wh = reinterpret_cast<uint16_t*>(wv);
+        for (int k = 0; k < 4; ++k) {
+            const uint4 x = reinterpret_cast<const uint4*>(wp)[k];
+            wv[4 * k + 0] = x.x;
+            wv[4 * k + 1] = x.y;
+            wv[4 * k + 2] = x.z;
+            wv[4 * k + 3] = x.w;
+        }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             const unsigned long long blk = (g0 >> 2) + b;
             uint32_t c[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), mf.step_lo, mf.step_hi};
             philox4x32_10(c, mf.seed_lo, mf.seed_hi);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) wh[4 * b + e] = upd(wh[4 * b + e], v[4 * b + e], c[e]);
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t pair = wv[2 * b + h];
+                const uint32_t lo = upd(static_cast<uint16_t>(pair & 0xFFFFu), v[4 * b + 2 * h], c[2 * h]);
+                const uint32_t hi = upd(static_cast<uint16_t>(pair >> 16), v[4 * b + 2 * h + 1], c[2 * h + 1]);
+                wv[2 * b + h] = lo | (hi << 16);
+            }
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(wp)[k] = wv[k];
+        for (int k = 0; k < 4; ++k)
+            reinterpret_cast<uint4*>(wp)[k] = make_uint4(wv[4 * k + 0], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
     } else {
         unsigned long long cur = ~0ULL;
-        uint32_t c[4] = {0, 0, 0, 0};
-        for (int j = 0; j < ncol; ++j) {
-            const unsigned long long gi = g0 + j;
-            if ((gi >> 2) != cur) {
-                cur = gi >> 2;
-                c[0] = static_cast<uint32_t>(cur);
-                c[1] = static_cast<uint32_t>(cur >> 32);
-                c[2] = mf.step_lo;
-                c[3] = mf.step_hi;
-                philox4x32_10(c, mf.seed_lo, mf.seed_hi);
+        uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < ncol) {
+                const unsigned long long gi = g0 + j;
+                if ((gi >> 2) != cur) {
+                    cur = gi >> 2;
+                    uint32_t c[4] = {static_cast<uint32_t>(cur), static_cast<uint32_t>(cur >> 32), mf.step_lo,
+                                     mf.step_hi};
+                    philox4x32_10(c, mf.seed_lo, mf.seed_hi);
+                    c0 = c[0];
+                    c1 = c[1];
+                    c2 = c[2];
+                    c3 = c[3];
+                }
+                const uint32_t e = static_cast<uint32_t>(gi & 3);
+                const uint32_t u = e == 0 ? c0 : (e == 1 ? c1 : (e == 2 ? c2 : c3));
+                wp[j] = upd(wp[j], v[j], u);
             }
-            wp[j] = upd(wp[j], v[j], c[gi & 3]);
         }
     }
 }
