@@ -284,7 +284,7 @@ class ProgramBuilder {
     // the program is full (the next launch then depends on it by stream order).
     int phase(const ProblemSpec& p0, const ProblemSpec* p1, bool reverse) {
         const int need_probs = p1 ? 2 : 1;
-        if (prog_.nphase + 1 > kMaxPhases || prog_.nprob + need_probs > kMaxProblems || prog_.nmaps + 12 > kMaxMaps)
+        if (prog_.nphase + 1 > kMaxPhases || prog_.nprob + need_probs > kMaxProblems || prog_.nmaps + 8 > kMaxMaps)
             RET(flush());
         GemmPhaseDesc& ph = prog_.phase[prog_.nphase];
         ph.prob_begin = prog_.nprob;
@@ -354,9 +354,15 @@ class ProgramBuilder {
         return idx >= 0 ? GNS_OK : (idx == -1 ? fail(GNS_ERR_INVALID, "tensor map table full") : GNS_ERR_INVALID);
     }
 
-    int output(const Mat& x, int& idx) {
-        idx = map_index(x, 32, 32, x.f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-        return idx >= 0 ? GNS_OK : (idx == -1 ? fail(GNS_ERR_INVALID, "tensor map table full") : GNS_ERR_INVALID);
+    // Outputs are written by the epilogue's own stores in 16-byte pieces.
+    static int output(const Mat& x, OutView& o) {
+        const size_t es = x.f32 ? 4 : 2;
+        if (reinterpret_cast<uintptr_t>(x.p) % 16 != 0 || (x.ld * es) % 16 != 0 || (x.stride * es) % 16 != 0)
+            return fail(GNS_ERR_INVALID, "outputs need 16-byte aligned rows");
+        o.p = x.p;
+        o.ld = x.ld;
+        o.stride = x.stride;
+        return GNS_OK;
     }
 
     int set_problem(GemmProblem& pr, const ProblemSpec& sp) {
@@ -369,17 +375,19 @@ class ProgramBuilder {
         if (sp.D2 && sp.Dt && !sp.D2t) return fail(GNS_ERR_INVALID, "second output needs its transposed map");
         if (sp.D.f32 && (sp.Dt || sp.D2)) return fail(GNS_ERR_INVALID, "fp32 output supports no transposed/second output");
         if (G_ > 65535) return fail(GNS_ERR_INVALID, "too many matrices in one launch");
-        pr.mA = pr.mB = pr.mD = pr.mDt = pr.mD2 = pr.mD2t = pr.mAt = pr.mBt = -1;
+        pr.mA = pr.mB = pr.mC = pr.mAt = pr.mBt = -1;
         if ((sp.a_sym || sp.b_sym || sp.lower) && bn != 128 * cg)
             return fail(GNS_ERR_INVALID, "lower-only storage needs square tiles");
         if ((sp.a_sym && sp.a_mn) || (sp.b_sym && sp.b_mn)) return fail(GNS_ERR_INVALID, "lower-only operands are K-major");
-        RET(operand(sp.A, sp.a_mn ? 64u : 128u, pr.mA, sp.a_mn));
+        const bool share = ts_.np == 2 && (!sp.sym || share_symmetric());
+        // With two pairs sharing A, each pair loads 64 of a CTA's 128 A rows.
+        RET(operand(sp.A, (sp.a_mn || share) ? 64u : 128u, pr.mA, sp.a_mn));
         RET(operand(sp.B, sp.b_mn ? 64u : static_cast<uint32_t>(bn / cg), pr.mB, sp.b_mn));
         if (sp.muon) {
             if (sp.sym || sp.Dt || sp.D2) return fail(GNS_ERR_INVALID, "the fused update needs a plain product");
             pr.muon = *sp.muon;
         } else {
-            RET(output(sp.D, pr.mD));
+            RET(output(sp.D, pr.d));
         }
         int flags = 0;
         if (sp.sym) flags |= kFlagSym;
@@ -396,22 +404,24 @@ class ProgramBuilder {
         }
         if (sp.lower) flags |= kFlagLower;
         if (sp.muon) flags |= kFlagMuon;
-        const bool share = ts_.np == 2 && (!sp.sym || share_symmetric());
         if (share) flags |= kFlagShareA;
         if (sp.C) {
             flags |= kFlagC;
             pr.C = static_cast<const __half*>(sp.C->p);
             pr.ldc = sp.C->ld;
             pr.strideC = sp.C->stride;
+            // The epilogue reads C in 32 x 32 blocks by TMA.
+            pr.mC = map_index(*sp.C, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+            if (pr.mC < 0) return pr.mC == -1 ? fail(GNS_ERR_INVALID, "tensor map table full") : GNS_ERR_INVALID;
         }
         if (sp.Dt) {
             flags |= kFlagDt;
-            RET(output(*sp.Dt, pr.mDt));
+            RET(output(*sp.Dt, pr.dt));
         }
         if (sp.D2) {
             flags |= kFlagD2;
-            RET(output(*sp.D2, pr.mD2));
-            if (sp.D2t) RET(output(*sp.D2t, pr.mD2t));
+            RET(output(*sp.D2, pr.d2));
+            if (sp.D2t) RET(output(*sp.D2t, pr.d2t));
         }
         pr.alpha = sp.alpha;
         pr.beta = sp.beta;

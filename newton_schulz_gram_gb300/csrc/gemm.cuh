@@ -59,10 +59,19 @@ constexpr int kMaxMaps = 64;
 constexpr int kMaxProblems = 48;
 constexpr int kMaxPhases = 40;
 
+// An output written by the epilogue: G row-major matrices, element (g, r, c)
+// at p + g stride + r ld (fp16, or fp32 for kFlagOutF32). ld is a multiple of
+// 16 bytes and p is 16-byte aligned, so rows are stored in 16-byte pieces.
+struct OutView {
+    void* p;
+    long long ld, stride;
+};
+
 struct GemmProblem {
     const __half* C;  // addend, row-major [G][M][ldc]
     long long ldc;
     long long strideC;
+    OutView d, dt, d2, d2t;  // D, its transpose, D2 and its transpose
     float alpha, beta, delta, gamma;
     int M, N, K;
     int tiles_n;           // tile columns of the matrix
@@ -71,9 +80,9 @@ struct GemmProblem {
     int flags;
     // Indices into GemmProgram::maps (-1 when unused). K-major operand maps:
     // box {64 (K), rows per CTA}; MN-major operand maps: box {64 (M or N),
-    // 64 (K)}; both 128-byte swizzle. Output maps: box {32, 32}, 64-byte
-    // swizzle (fp16) or 128-byte swizzle (fp32).
-    int mA, mB, mD, mDt, mD2, mD2t;
+    // 64 (K)}; both 128-byte swizzle. The addend's map (mC): box {32, 32},
+    // 64-byte swizzle.
+    int mA, mB, mC;
     int mAt, mBt;  // MN-major views (box {64, 64}) of lower-only A / B
     MuonFuse muon;
 };

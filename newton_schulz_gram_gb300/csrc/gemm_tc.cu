@@ -9,11 +9,14 @@
 //               tcgen05.mma.cta_group::1.kind::f16 (M = 128, N = BN, K = 16)
 //               into one of two TMEM accumulators (2 x BN fp32 columns), so
 //               the epilogue of tile i overlaps the MMAs of tile i + 1.
-//   warps 2-5   epilogue: tcgen05.ld of 32 x 32 sub-blocks, the fp32 epilogue
+//   warps 2-9   epilogue: tcgen05.ld of 32 x 32 sub-blocks, the fp32 epilogue
 //               alpha * acc + beta * C (+ the second output delta * v + gamma I),
-//               then TMA stores of the sub-block and, when asked, of its
-//               transpose (the mirror write of the symmetric product, Dion3 §5
-//               "Epilogue: Writing to the Transposed Tile").
+//               then the sub-block and, when asked, its transpose (the mirror
+//               write of the symmetric product, Dion3 §5 "Epilogue: Writing to
+//               the Transposed Tile") are staged in shared memory and written
+//               to global memory by the warp's own coalesced stores (8 rows of
+//               64 bytes per instruction), so the epilogue never waits on the
+//               TMA unit, which the operand loads keep busy.
 //
 // Symmetric products (Dion3 §5 "Triangular Scheduler", App. C.1) visit only
 // the 128 x BN tiles that touch the lower triangle (row block i holds the
@@ -25,7 +28,7 @@
 // result is exactly symmetric.
 //
 // Transposed sub-blocks are built in shared memory with ldmatrix.trans /
-// stmatrix; all fp16 staging uses the 64-byte swizzle of its TMA maps.
+// stmatrix; fp16 staging uses a 64-byte swizzle, fp32 staging a 128-byte one.
 #include <cstdio>
 
 #include "gemm.cuh"
@@ -41,12 +44,13 @@ static_assert(sizeof(GemmProgram) <= 32764, "kernel parameter block too large");
 constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 
-// One per-warp epilogue staging buffer (bytes): a 32 x 32 fp16 block and its
-// transpose, or one 32 x 32 fp32 block. A second output reuses it in a
-// second pass.
-constexpr int SBUF = 4096;
-constexpr int kOffD = 0;
-constexpr int kOffDt = 2048;
+// Per-warp epilogue shared memory: three 2 KB slots of 32 rows x 64 bytes
+// (64-byte swizzle). Slots 0 and 1 receive, by TMA, the C addend of the
+// warp's next two 32 x 32 blocks; once a block's C has been read, its slot
+// stages that block's output for the coalesced stores. Slot 2 holds the
+// transposed block of a mirrored or diagonal sub-block.
+constexpr int kSlot = 2048;
+constexpr int SBUF = 3 * kSlot;
 
 // Kernel variants: <BN, CG>. CG = 1: one CTA computes a 128 x BN tile.
 // CG = 2: a cluster of two CTAs computes a 256 x BN tile with paired MMAs
@@ -56,22 +60,38 @@ template <int BN, int CG>
 struct Cfg;
 template <>
 struct Cfg<128, 1> {
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = 5;
 };
 template <>
 struct Cfg<256, 1> {
-    static constexpr int STAGES = 4;
+    static constexpr int STAGES = 3;
 };
 template <>
 struct Cfg<256, 2> {
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = 5;
 };
+
+// Tile-walk tables, copied from the kernel parameters into shared memory at
+// start: every role decodes every tile it visits, and parameter-space loads
+// with a tile-dependent index are slow under load.
+struct CtlPhase {
+    int tile_begin, tiles_per_matrix, prob_begin, reverse, wait_tiles;
+};
+struct CtlProb {
+    int tiles_per_matrix, tiles_n, tiles_n_walk, flags, K;
+    int mA, mB, mAt, mBt, mC;
+};
+constexpr int kCtlBytes = kMaxPhases * static_cast<int>(sizeof(CtlPhase)) + kMaxProblems * static_cast<int>(sizeof(CtlProb));
+__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 5 + 2 * kEpiWarps; }
 
 template <int BN, int CG>
 constexpr int smem_bytes() {
     return 1024 + Cfg<BN, CG>::STAGES * (BM * BK * 2 + (BN / CG) * BK * 2) + kEpiWarps * SBUF +
-           (2 * Cfg<BN, CG>::STAGES + 5) * 8 + 16;
+           kNumBars(Cfg<BN, CG>::STAGES) * 8 + 16 + kCtlBytes;
 }
+static_assert(smem_bytes<256, 2>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<128, 1>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<256, 1>() <= 232448, "shared memory budget");
 
 struct TileInfo {
     int p, g, m0, n0, s;  // problem, matrix, tile origin, phase
@@ -85,39 +105,111 @@ __host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int
     return share ? c + (c & 1) : c;
 }
 
+// Decodes program tiles for one role. Every role visits its tiles in
+// increasing order, and phases change only a few dozen times per program, so
+// the walker keeps the current phase and its (at most two) problems in
+// registers and reads the shared-memory tables only when the phase changes:
+// under load a shared-memory read costs hundreds of cycles.
 template <int BN, int CG>
-__device__ __forceinline__ TileInfo decode_tile(const GemmProgram& P, int tile) {
+struct TileWalker {
+    static constexpr int TM = BM * CG;
+    const CtlPhase* cph;
+    const CtlProb* cpb;
+    int nphase, G;
+    int s = -1, next_begin = 0;  // current phase and the first tile of the next one
+    CtlPhase ph{};
+    CtlProb pb[2]{};             // the phase's problems
+    int cur = 0;                 // which of pb[] the last decoded tile belongs to
+
+    __device__ __forceinline__ TileWalker(const CtlPhase* a, const CtlProb* b, int np, int g)
+        : cph(a), cpb(b), nphase(np), G(g) {}
+
+    __device__ __forceinline__ const CtlProb& prob() const { return cur ? pb[1] : pb[0]; }
+
+    __device__ __forceinline__ TileInfo decode(int tile) {
+        if (tile >= next_begin) {
+            while (s + 1 < nphase && tile >= cph[s + 1].tile_begin) ++s;
+            ph = cph[s];
+            next_begin = s + 1 < nphase ? cph[s + 1].tile_begin : 0x7fffffff;
+            pb[0] = cpb[ph.prob_begin];
+            if (ph.tiles_per_matrix > pb[0].tiles_per_matrix) pb[1] = cpb[ph.prob_begin + 1];
+        }
+        const int local = tile - ph.tile_begin;
+        int g = local / ph.tiles_per_matrix;
+        int t = local - g * ph.tiles_per_matrix;
+        if (ph.reverse) g = G - 1 - g;
+        cur = t >= pb[0].tiles_per_matrix ? 1 : 0;
+        if (cur) t -= pb[0].tiles_per_matrix;
+        const CtlProb& pr = prob();
+        const int flags = pr.flags;
+        int i, j;
+        // Tiles past the real ones (padding) decode to out-of-range tiles: their
+        // loads read zeros and their epilogue writes nothing.
+        if ((flags & kFlagSym) && TM == BN && !(flags & kFlagShareA)) {
+            // Square tiles: row block i holds i + 1 tiles, i (i + 1) / 2 before it.
+            i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
+            while (i * (i + 1) / 2 > t) --i;
+            while ((i + 1) * (i + 2) / 2 <= t) ++i;
+            j = t - i * (i + 1) / 2;
+        } else if (flags & kFlagSym) {
+            const bool share = flags & kFlagShareA;
+            int acc = 0;
+            i = 0;
+            while (true) {
+                const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n, share);
+                if (t < acc + cnt) break;
+                acc += cnt;
+                ++i;
+            }
+            j = t - acc;
+        } else {
+            i = t / pr.tiles_n_walk;
+            j = t - i * pr.tiles_n_walk;
+        }
+        return TileInfo{ph.prob_begin + cur, g, i * TM, j * BN, s};
+    }
+};
+
+// The same decode straight from the shared-memory tables, resuming the phase
+// search at `s` (used where registers are scarce).
+template <int BN, int CG>
+__device__ __forceinline__ TileInfo decode_tile(const CtlPhase* cph, const CtlProb* cpb, int nphase, int G, int tile,
+                                                int& s) {
     constexpr int TM = BM * CG;
-    int s = 0;
-    while (s + 1 < P.nphase && tile >= P.phase[s + 1].tile_begin) ++s;
-    const GemmPhaseDesc& ph = P.phase[s];
+    while (s + 1 < nphase && tile >= cph[s + 1].tile_begin) ++s;
+    const CtlPhase ph = cph[s];
     const int local = tile - ph.tile_begin;
     int g = local / ph.tiles_per_matrix;
     int t = local - g * ph.tiles_per_matrix;
-    if (ph.reverse) g = P.G - 1 - g;
+    if (ph.reverse) g = G - 1 - g;
     int p = ph.prob_begin;
-    while (t >= P.prob[p].tiles_per_matrix) {
-        t -= P.prob[p].tiles_per_matrix;
+    while (t >= cpb[p].tiles_per_matrix) {
+        t -= cpb[p].tiles_per_matrix;
         ++p;
     }
-    const GemmProblem& pr = P.prob[p];
+    const int flags = cpb[p].flags;
     int i, j;
-    // Tiles past the real ones (padding) decode to out-of-range tiles: their
-    // loads read zeros and their epilogue writes nothing.
-    if (pr.flags & kFlagSym) {
-        const bool share = pr.flags & kFlagShareA;
+    if ((flags & kFlagSym) && TM == BN && !(flags & kFlagShareA)) {
+        i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
+        while (i * (i + 1) / 2 > t) --i;
+        while ((i + 1) * (i + 2) / 2 <= t) ++i;
+        j = t - i * (i + 1) / 2;
+    } else if (flags & kFlagSym) {
+        const bool share = flags & kFlagShareA;
+        const int tiles_n = cpb[p].tiles_n;
         int acc = 0;
         i = 0;
         while (true) {
-            const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n, share);
+            const int cnt = sym_row_tiles(i, TM, BN, tiles_n, share);
             if (t < acc + cnt) break;
             acc += cnt;
             ++i;
         }
         j = t - acc;
     } else {
-        i = t / pr.tiles_n_walk;
-        j = t - i * pr.tiles_n_walk;
+        const int wn = cpb[p].tiles_n_walk;
+        i = t / wn;
+        j = t - i * wn;
     }
     return TileInfo{p, g, i * TM, j * BN, s};
 }
@@ -129,10 +221,9 @@ constexpr uint32_t kMnBlockBytes = 64 * BK * 2;
 // One k-block of one operand into shared memory: a K-major tile is one box
 // {64 (K), rows}; an MN-major tile is rows / 64 boxes {64 (M or N), 64 (K)}.
 // mode 0: this CTA's own barrier; 1: the pair leader's barrier (bar is a
-// cluster address); 2: multicast to the CTAs in `mask`, completing on the
-// pair leader's barrier of each destination.
+// cluster address).
 __device__ __forceinline__ void load_operand(int mode, uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn,
-                                             int row0, int rows, int kb, int g, uint16_t mask) {
+                                             int row0, int rows, int kb, int g) {
     const int boxes = mn ? rows / 64 : 1;
     for (int h = 0; h < boxes; ++h) {
         const uint32_t d = dst + h * kMnBlockBytes;
@@ -140,10 +231,8 @@ __device__ __forceinline__ void load_operand(int mode, uint32_t dst, const CUten
         const int c1 = mn ? kb * BK : row0;
         if (mode == 0)
             tma_load_3d(d, map, bar, c0, c1, g);
-        else if (mode == 1)
-            tma_load_3d_pair(d, map, bar, c0, c1, g);
         else
-            tma_load_3d_multicast_pair(d, map, bar, c0, c1, g, mask);
+            tma_load_3d_pair(d, map, bar, c0, c1, g);
     }
 }
 
@@ -153,24 +242,29 @@ __device__ __forceinline__ uint32_t sw64_addr(uint32_t base, int row, int col) {
     return base + row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4) + (col & 7) * 2;
 }
 
+// Address of 16-byte piece k of row r in a 64B-swizzled block of 64-byte rows.
+__device__ __forceinline__ uint32_t sw64_piece(uint32_t base, int r, int k) {
+    return base + r * 64 + (((k ^ (r >> 1)) & 3) << 4);
+}
+
 // Row `lane` (32 values) of a 64B-swizzled fp16 block.
 __device__ __forceinline__ void stage_row_f16(uint32_t base, int lane, const float (&v)[32]) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t addr = base + lane * 64 + (((k ^ (lane >> 1)) & 3) << 4);
-        st_shared_v4(addr, pack_half2(v[8 * k + 0], v[8 * k + 1]), pack_half2(v[8 * k + 2], v[8 * k + 3]),
-                     pack_half2(v[8 * k + 4], v[8 * k + 5]), pack_half2(v[8 * k + 6], v[8 * k + 7]));
-    }
+    for (int k = 0; k < 4; ++k)
+        st_shared_v4(sw64_piece(base, lane, k), pack_half2(v[8 * k + 0], v[8 * k + 1]),
+                     pack_half2(v[8 * k + 2], v[8 * k + 3]), pack_half2(v[8 * k + 4], v[8 * k + 5]),
+                     pack_half2(v[8 * k + 6], v[8 * k + 7]));
 }
 
-// Row `lane` of a 128B-swizzled fp32 block.
-__device__ __forceinline__ void stage_row_f32(uint32_t base, int lane, const float (&v)[32]) {
+// Columns 16 H .. 16 H + 15 of row `lane` as one 64-byte fp32 row of a
+// 64B-swizzled block.
+template <int H>
+__device__ __forceinline__ void stage_row_f32_half(uint32_t base, int lane, const float (&v)[32]) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t addr = base + lane * 128 + (((k ^ lane) & 7) << 4);
-        st_shared_v4(addr, __float_as_uint(v[4 * k + 0]), __float_as_uint(v[4 * k + 1]),
-                     __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
-    }
+    for (int k = 0; k < 4; ++k)
+        st_shared_v4(sw64_piece(base, lane, k), __float_as_uint(v[16 * H + 4 * k + 0]),
+                     __float_as_uint(v[16 * H + 4 * k + 1]), __float_as_uint(v[16 * H + 4 * k + 2]),
+                     __float_as_uint(v[16 * H + 4 * k + 3]));
 }
 
 // dst = src^T for a 32 x 32 fp16 block (both 64B-swizzled): 8 x 8 block (R, i)
@@ -200,24 +294,39 @@ __device__ __forceinline__ void merge_upper(uint32_t d, uint32_t dt, int lane) {
     }
 }
 
-// Row `grow` of C, columns c0 .. c0 + 31, as 16 packed fp16 pairs.
-__device__ __forceinline__ void load_c(const GemmProblem& pr, int g, int grow, int c0, uint4 (&cb)[4]) {
-    if (grow >= pr.M) {
+// Writes a staged block of 32 rows x 64 bytes (64B-swizzled, elements of ES
+// bytes) to rows r0 .. r0 + 31 and the 64 / ES columns from c0 of matrix g
+// of `o`, clipped to rows x cols. Instruction j stores rows 8 j .. 8 j + 7,
+// four lanes per 64-byte row segment.
+template <int ES>
+__device__ __forceinline__ void store_rows64(uint32_t stg, const OutView& o, int g, int r0, int c0, int rows, int cols,
+                                             int lane) {
+    constexpr int EPP = 16 / ES;  // elements per 16-byte piece
+    const int k = lane & 3;
+    const int gc = c0 + EPP * k;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cb[k] = make_uint4(0, 0, 0, 0);
-        return;
-    }
-    const __half* crow = pr.C + static_cast<long long>(g) * pr.strideC + static_cast<long long>(grow) * pr.ldc + c0;
-    if (c0 + 32 <= pr.N) {
+    for (int j = 0; j < 4; ++j) {
+        const int r = 8 * j + (lane >> 2);
+        const uint4 v = ld_shared_v4(sw64_piece(stg, r, k));
+        const int gr = r0 + r;
+        if (gr >= rows || gc >= cols) continue;
+        uint8_t* p = static_cast<uint8_t*>(o.p) +
+                     (static_cast<long long>(g) * o.stride + static_cast<long long>(gr) * o.ld + gc) * ES;
+        if (gc + EPP <= cols) {
+            *reinterpret_cast<uint4*>(p) = v;
+        } else {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            if constexpr (ES == 2) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cb[k] = *reinterpret_cast<const uint4*>(crow + 8 * k);
-    } else {
-        uint16_t h[32];
-        for (int j = 0; j < 32; ++j) h[j] = (c0 + j < pr.N) ? reinterpret_cast<const uint16_t*>(crow)[j] : 0;
+                for (int e = 0; e < 8; ++e)
+                    if (gc + e < cols)
+                        reinterpret_cast<uint16_t*>(p)[e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+            } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            cb[k] = make_uint4(h[8 * k] | (uint32_t(h[8 * k + 1]) << 16), h[8 * k + 2] | (uint32_t(h[8 * k + 3]) << 16),
-                               h[8 * k + 4] | (uint32_t(h[8 * k + 5]) << 16), h[8 * k + 6] | (uint32_t(h[8 * k + 7]) << 16));
+                for (int e = 0; e < 4; ++e)
+                    if (gc + e < cols) reinterpret_cast<uint32_t*>(p)[e] = w[e];
+            }
+        }
     }
 }
 
@@ -320,13 +429,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint8_t* sB = sA + STAGES * A_BYTES;
     uint8_t* sEpi = sB + STAGES * B_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiWarps * SBUF);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars(STAGES));
+    CtlPhase* cph = reinterpret_cast<CtlPhase*>(tmem_slot + 4);
+    CtlProb* cpb = reinterpret_cast<CtlProb*>(cph + kMaxPhases);
 
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
     const uint32_t accf0 = smem_u32(bars + 2 * STAGES);
     const uint32_t acce0 = smem_u32(bars + 2 * STAGES + 2);
     const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+    const uint32_t cbar0 = smem_u32(bars + 2 * STAGES + 5);  // two C-slot barriers per epilogue warp
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -338,6 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int unit = blockIdx.x / CL;                        // this cluster's tile walker
     const int units = gridDim.x / CL;
     const int nwalk = P.total_tiles / NP;                    // super-tiles: NP consecutive tiles
+    const int nphase = P.nphase;
+    const int G = P.G;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -351,13 +465,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             mbar_init(acce0 + 8 * b, kEpiWarps * CG);
         }
         mbar_init(drain_bar, 1);
+        for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(cbar0 + 8 * b, 1);
         fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < nphase; i += blockDim.x) {
+        const GemmPhaseDesc& ph = P.phase[i];
+        cph[i] = CtlPhase{ph.tile_begin, ph.tiles_per_matrix, ph.prob_begin, ph.reverse, ph.wait_tiles};
+    }
+    for (int i = threadIdx.x; i < P.nprob; i += blockDim.x) {
+        const GemmProblem& pr = P.prob[i];
+        cpb[i] = CtlProb{pr.tiles_per_matrix, pr.tiles_n, pr.tiles_n_walk, pr.flags, pr.K,
+                         pr.mA, pr.mB, pr.mAt, pr.mBt, pr.mC};
     }
     if (warp == 0 && lane == 0) {
         for (int m = 0; m < P.nmaps; ++m) prefetch_tmap(&P.maps[m]);
     }
     // Counter value at which every tile of the phases before phase s is done.
-    auto dep_target = [&](int s) { return P.phase[s].wait_tiles * (kEpiWarps * CG); };
+    auto dep_target = [&](int s) { return cph[s].wait_tiles * (kEpiWarps * CG); };
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish<CG>();
@@ -378,9 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
+            TileWalker<BN, CG> walk(cph, cpb, nphase, G);
             for (int w = unit; w < nwalk && ok; w += units) {
-                const TileInfo t = decode_tile<BN, CG>(P, w * NP + pair);
-                const GemmProblem& pr = P.prob[t.p];
+                const TileInfo t = walk.decode(w * NP + pair);
+                const CtlProb& pr = walk.prob();
                 const CUtensorMap* mapA = &P.maps[pr.mA];
                 const CUtensorMap* mapB = &P.maps[pr.mB];
                 const bool a_mn0 = pr.flags & kFlagAmn;
@@ -392,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const int ti = t.m0 / TM, tj = t.n0 / TM;
                 const bool share = (NP == 2) && (pr.flags & kFlagShareA);
                 const int kblocks = (pr.K + BK - 1) / BK;
-                if (P.counters && P.phase[t.s].wait_tiles > 0) {
+                if (P.counters && t.s > 0) {
                     // The operands of this phase are outputs of earlier phases on
                     // the same matrix, stored by other CTAs.
                     if (!wait_counter(P.counters + t.g, dep_target(t.s), err)) break;
@@ -417,22 +542,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     const CUtensorMap* mB_k = b_t ? mapBt : mapB;
                     if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-                        load_operand(0, smem_u32(sA + stage * A_BYTES), mA_k, fb, a_mn, arow, BM, kb, t.g, 0);
-                        load_operand(0, smem_u32(sB + stage * B_BYTES), mB_k, fb, b_mn, brow, BNH, kb, t.g, 0);
+                        load_operand(0, smem_u32(sA + stage * A_BYTES), mA_k, fb, a_mn, arow, BM, kb, t.g);
+                        load_operand(0, smem_u32(sB + stage * B_BYTES), mB_k, fb, b_mn, brow, BNH, kb, t.g);
                     } else {
-                        // All halves complete on the pair leader's barrier. A
-                        // shared A half is loaded once by the first pair and
-                        // multicast to the same-rank CTA of both pairs.
+                        // All halves complete on the pair leader's barrier.
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (A_BYTES + B_BYTES));
                         const uint32_t lead_fb = map_to_rank(fb, lead);
                         if (!share) {
-                            load_operand(1, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g, 0);
-                        } else if (pair == 0) {
+                            load_operand(1, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g);
+                        } else {
+                            // The two pairs need the same 128 A rows in their
+                            // same-rank CTAs: each pair loads one 64-row half
+                            // (one 64 x 64 box, 8 KB) and multicasts it to both,
+                            // so every CTA issues the same number of bytes.
                             const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2 + rank)));
-                            load_operand(2, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g,
-                                         mask);
+                            const int r = arow + 64 * pair;
+                            tma_load_3d_multicast_pair(smem_u32(sA + stage * A_BYTES) + pair * kMnBlockBytes, mA_k,
+                                                       lead_fb, a_mn ? r : kb * BK, a_mn ? kb * BK : r, t.g, mask);
                         }
-                        load_operand(1, smem_u32(sB + stage * B_BYTES), mB_k, lead_fb, b_mn, brow, BNH, kb, t.g, 0);
+                        load_operand(1, smem_u32(sB + stage * B_BYTES), mB_k, lead_fb, b_mn, brow, BNH, kb, t.g);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -464,15 +592,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             bool ok = true;
             constexpr uint16_t kStageMask = (NP == 2) ? 0xF : 0x3;  // both pairs' CTAs
             const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
+            TileWalker<BN, CG> walk(cph, cpb, nphase, G);
             for (int w = unit; w < nwalk && ok; w += units, ++iter) {
-                const TileInfo t = decode_tile<BN, CG>(P, w * NP + pair);
-                const GemmProblem& pr = P.prob[t.p];
-                const int kblocks = (pr.K + BK - 1) / BK;
+                const TileInfo t = walk.decode(w * NP + pair);
+                const int pflags = walk.prob().flags;
+                const int kblocks = (walk.prob().K + BK - 1) / BK;
                 const int buf = iter & 1;
-                const bool a_mn0 = pr.flags & kFlagAmn;
-                const bool b_mn0 = pr.flags & kFlagBmn;
-                const bool a_sym = pr.flags & kFlagAsym;
-                const bool b_sym = pr.flags & kFlagBsym;
+                const bool a_mn0 = pflags & kFlagAmn;
+                const bool b_mn0 = pflags & kFlagBmn;
+                const bool a_sym = pflags & kFlagAsym;
+                const bool b_sym = pflags & kFlagBsym;
                 const int ti = t.m0 / TM, tj = t.n0 / TM;
                 if (!mbar_wait(acce0 + 8 * buf, ((iter >> 1) & 1) ^ 1, err)) break;
                 tc_fence_after();
@@ -527,47 +656,89 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int ew = warp - 2;                // epilogue warp 0..7
         constexpr int CPW = NCH / 2;            // chunks per warp: two warps share a quarter
         const int cbeg = (ew >> 2) * CPW;       // this warp's first chunk
-        const uint32_t stg = smem_u32(sEpi + ew * SBUF);
+        const uint32_t wbase = smem_u32(sEpi + ew * SBUF);
+        const uint32_t sT = wbase + 2 * kSlot;  // transposed block
+        const uint32_t cbw = cbar0 + 16 * ew;   // barrier of C slot k: cbw + 8 k
         const uint32_t acce_lead = (CG == 2) ? map_to_rank(acce0, lead) : acce0;
+        uint32_t cpar = 0;  // bit k: parity of C slot k's next completion
+        uint32_t cpend = 0; // bit k: a C load into slot k is in flight
         int iter = 0;
-        for (int w = unit; w < nwalk; w += units, ++iter) {
-            const TileInfo t = decode_tile<BN, CG>(P, w * NP + pair);
+        bool ok = true;
+        int ps = 0;
+        for (int w = unit; w < nwalk && ok; w += units, ++iter) {
+            const TileInfo t = decode_tile<BN, CG>(cph, cpb, nphase, G, w * NP + pair, ps);
             const GemmProblem& pr = P.prob[t.p];
             const int buf = iter & 1;
-            const int flags = pr.flags;
+            const int flags = cpb[t.p].flags;
             const bool sym = flags & kFlagSym;
             const bool hasC = flags & kFlagC;
             const bool f32 = flags & kFlagOutF32;
+            const int M = pr.M, N = pr.N;
             const int r0 = t.m0 + BM * static_cast<int>(rank) + q * 32;
             const int grow = r0 + lane;
-            const bool rows_live = r0 < pr.M;
             const int sr = r0 >> 5;
-            auto active = [&](int c) {
-                const int c0 = t.n0 + 32 * c;
-                return rows_live && c0 < pr.N && !(sym && (c0 >> 5) > sr);
-            };
-            const int cend = cbeg + CPW;
-            int c = cbeg;
-            while (c < cend && !active(c)) ++c;
-            if (hasC && P.counters && P.phase[t.s].wait_tiles > 0) {
-                // C is an earlier phase's output: acquire it like the producer.
-                if (!wait_counter(P.counters + t.g, dep_target(t.s), err)) break;
+            // This warp's live 32 x 32 blocks of the tile, in order (bit c - cbeg).
+            uint32_t am = 0;
+            if (r0 < M) {
+#pragma unroll
+                for (int c = 0; c < CPW; ++c) {
+                    const int c0 = t.n0 + 32 * (cbeg + c);
+                    if (c0 < N && !(sym && (c0 >> 5) > sr)) am |= 1u << c;
+                }
             }
-            uint4 cb[4];
-            if (hasC && c < cend) load_c(pr, t.g, grow, t.n0 + 32 * c, cb);
+            const CUtensorMap* mapC = &P.maps[cpb[t.p].mC];
+            // C of block k of the list into slot k & 1 (lane 0 issues).
+            auto load_c = [&](int k, int c) {
+                const uint32_t bar = cbw + 8 * (k & 1);
+                mbar_arrive_expect_tx(bar, kSlot);
+                tma_load_3d(wbase + (k & 1) * kSlot, mapC, bar, t.n0 + 32 * c, r0, t.g);
+            };
+            if (hasC && am) {
+                if (P.counters && t.s > 0) {
+                    // C is an earlier phase's output: acquire it like the producer.
+                    int okc = 1;
+                    if (lane == 0) okc = wait_counter(P.counters + t.g, dep_target(t.s), err) ? 1 : 0;
+                    if (!__shfl_sync(0xffffffffu, okc, 0)) break;
+                }
+                uint32_t m = am;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    if (m) {
+                        if (lane == 0) {
+                            if (k == 0) fence_proxy_async_global();
+                            load_c(k, cbeg + __ffs(m) - 1);
+                        }
+                        cpend |= 1u << k;
+                        m &= m - 1;
+                    }
+                }
+            }
 
-            if (!mbar_wait(accf0 + 8 * buf, (iter >> 1) & 1, err)) break;
+            int okw = mbar_wait(accf0 + 8 * buf, (iter >> 1) & 1, err) ? 1 : 0;
+            if (!okw) break;
             tc_fence_after();
 
+            uint32_t m = am;
+            int k = 0;
 #pragma unroll 1
-            while (c < cend) {
+            while (m) {
+                const int c = cbeg + __ffs(m) - 1;
+                m &= m - 1;
                 const int c0 = t.n0 + 32 * c;
+                const uint32_t slot = wbase + (k & 1) * kSlot;
                 uint32_t acc[32];
                 tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c * 32, acc);
-                int cn = c + 1;
-                while (cn < cend && !active(cn)) ++cn;
-                uint4 cbn[4];
-                if (hasC && cn < cend) load_c(pr, t.g, grow, t.n0 + 32 * cn, cbn);
+                uint4 cb[4];
+                if (hasC) {
+                    if (!mbar_wait(cbw + 8 * (k & 1), (cpar >> (k & 1)) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    cpar ^= 1u << (k & 1);
+                    cpend &= ~(1u << (k & 1));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) cb[kk] = ld_shared_v4(sw64_piece(slot, lane, kk));
+                }
                 tmem_ld_wait();
 
                 float v[32];
@@ -575,64 +746,68 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 for (int j = 0; j < 32; ++j) v[j] = pr.alpha * __uint_as_float(acc[j]);
                 if (hasC) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t w[4] = {cb[k].x, cb[k].y, cb[k].z, cb[k].w};
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t wv[4] = {cb[kk].x, cb[kk].y, cb[kk].z, cb[kk].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                            v[8 * k + 2 * e] = fmaf(pr.beta, f.x, v[8 * k + 2 * e]);
-                            v[8 * k + 2 * e + 1] = fmaf(pr.beta, f.y, v[8 * k + 2 * e + 1]);
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+                            v[8 * kk + 2 * e] = fmaf(pr.beta, f.x, v[8 * kk + 2 * e]);
+                            v[8 * kk + 2 * e + 1] = fmaf(pr.beta, f.y, v[8 * kk + 2 * e + 1]);
                         }
                     }
                 }
+                // Every lane has read its C row: the slot may be overwritten.
+                __syncwarp();
                 if (flags & kFlagMuon) {
                     muon_update_row(pr, t.g, grow, c0, v);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) cb[k] = cbn[k];
-                    c = cn;
-                    continue;
-                }
-                const bool diag_block = sym && ((c0 >> 5) == sr);
-                // Lower-only outputs mirror only inside diagonal tiles.
-                const bool mirror = (flags & kFlagDt) && !diag_block && (!(flags & kFlagLower) || t.m0 == t.n0);
-
-                // Stage, transpose (mirror or diagonal fix-up) and store one
-                // 32 x 32 block; the buffer is free once the previous stores
-                // have read it.
-                auto emit = [&](const float (&val)[32], int map_d, int map_dt) {
-                    if (lane == 0) bulk_wait_read<0>();
-                    __syncwarp();
-                    if (f32) {
-                        stage_row_f32(stg + kOffD, lane, val);
-                    } else {
-                        stage_row_f16(stg + kOffD, lane, val);
-                        if (mirror || diag_block) {
+                } else {
+                    const bool diag_block = sym && ((c0 >> 5) == sr);
+                    // Lower-only outputs mirror only inside diagonal tiles.
+                    const bool mirror = (flags & kFlagDt) && !diag_block && (!(flags & kFlagLower) || t.m0 == t.n0);
+                    // Stage, transpose (mirror or diagonal fix-up) and store one
+                    // 32 x 32 block; the slot is free again once the warp has
+                    // read it back.
+                    auto emit = [&](const float (&val)[32], const OutView& od, const OutView& odt) {
+                        if (f32) {
+                            stage_row_f32_half<0>(slot, lane, val);
                             __syncwarp();
-                            transpose_block(stg + kOffD, stg + kOffDt, lane);
-                            if (diag_block) {
+                            store_rows64<4>(slot, od, t.g, r0, c0, M, N, lane);
+                            __syncwarp();
+                            stage_row_f32_half<1>(slot, lane, val);
+                            __syncwarp();
+                            store_rows64<4>(slot, od, t.g, r0, c0 + 16, M, N, lane);
+                        } else {
+                            stage_row_f16(slot, lane, val);
+                            if (mirror || diag_block) {
                                 __syncwarp();
-                                merge_upper(stg + kOffD, stg + kOffDt, lane);
+                                transpose_block(slot, sT, lane);
+                                if (diag_block) {
+                                    __syncwarp();
+                                    merge_upper(slot, sT, lane);
+                                }
                             }
+                            __syncwarp();
+                            store_rows64<2>(slot, od, t.g, r0, c0, M, N, lane);
+                            if (mirror) store_rows64<2>(sT, odt, t.g, c0, r0, N, M, lane);
                         }
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&P.maps[map_d], stg + kOffD, c0, r0, t.g);
-                        if (mirror) tma_store_3d(&P.maps[map_dt], stg + kOffDt, r0, c0, t.g);
-                        bulk_commit();
-                    }
-                };
-                emit(v, pr.mD, pr.mDt);
-                if (flags & kFlagD2) {
+                        __syncwarp();
+                    };
+                    emit(v, pr.d, pr.dt);
+                    if (flags & kFlagD2) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = pr.delta * v[j] + ((grow == c0 + j) ? pr.gamma : 0.0f);
-                    emit(v, pr.mD2, pr.mD2t);
+                        for (int j = 0; j < 32; ++j) v[j] = pr.delta * v[j] + ((grow == c0 + j) ? pr.gamma : 0.0f);
+                        emit(v, pr.d2, pr.d2t);
+                    }
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) cb[k] = cbn[k];
-                c = cn;
+                // The C of the block two places further into the slot just freed.
+                if (hasC && m && (m & (m - 1))) {
+                    const uint32_t m2 = m & (m - 1);
+                    if (lane == 0) load_c(k, cbeg + __ffs(m2) - 1);
+                    cpend |= 1u << (k & 1);
+                }
+                ++k;
             }
+            if (!ok) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -640,16 +815,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     mbar_arrive(acce0 + 8 * buf);
                 else
                     mbar_arrive_cluster(acce_lead + 8 * buf);
-                if (P.counters) {
-                    // Publish this warp's part of the tile: stores complete,
-                    // then a release on the matrix's counter.
-                    bulk_wait_all();
-                    fence_proxy_async_global();
-                    red_release_add(P.counters + t.g, 1);
-                }
+                // Publish this warp's part of the tile: the release is
+                // cumulative over the lanes' stores, which the warp barrier
+                // above ordered before it.
+                if (P.counters) red_release_add(P.counters + t.g, 1);
             }
         }
-        if (lane == 0) bulk_wait_all();
+        // C loads still in flight (only after a failed wait) land before exit.
+        if (lane == 0) {
+            for (int kk = 0; kk < 2; ++kk)
+                if (cpend & (1u << kk)) drain_wait(cbw + 8 * kk, (cpar >> kk) & 1);
+        }
         __syncwarp();
     }
 
