@@ -105,27 +105,33 @@ __host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int
     return share ? c + (c & 1) : c;
 }
 
-// Decodes program tiles for one role. Every role visits its tiles in
-// increasing order, and phases change only a few dozen times per program, so
-// the walker keeps the current phase and its (at most two) problems in
-// registers and reads the shared-memory tables only when the phase changes:
-// under load a shared-memory read costs hundreds of cycles.
+// Decodes program tiles for one role. A role visits the tiles first,
+// first + step, first + 2 step, ...; phases change only a few dozen times per
+// program. The walker keeps the current phase and its (at most two) problems
+// in registers, reads the shared-memory tables only when the phase changes,
+// and within a phase advances the (matrix, tile) position by the fixed
+// stride instead of dividing: the decode runs on a single thread between
+// k-blocks, where every dependent instruction counts.
 template <int BN, int CG>
 struct TileWalker {
     static constexpr int TM = BM * CG;
     const CtlPhase* cph;
     const CtlProb* cpb;
-    int nphase, G;
+    int nphase, G, step;
     int s = -1, next_begin = 0;  // current phase and the first tile of the next one
     CtlPhase ph{};
     CtlProb pb[2]{};             // the phase's problems
+    float inv_wn[2]{};           // 1 / tiles_n_walk of each problem
+    int lg = 0, lt = 0;          // position of the last tile: matrix slot, tile within the matrix
+    int sq = 0, sr = 0;          // step = sq tiles_per_matrix + sr
     int cur = 0;                 // which of pb[] the last decoded tile belongs to
 
-    __device__ __forceinline__ TileWalker(const CtlPhase* a, const CtlProb* b, int np, int g)
-        : cph(a), cpb(b), nphase(np), G(g) {}
+    __device__ __forceinline__ TileWalker(const CtlPhase* a, const CtlProb* b, int np, int g, int stp)
+        : cph(a), cpb(b), nphase(np), G(g), step(stp) {}
 
     __device__ __forceinline__ const CtlProb& prob() const { return cur ? pb[1] : pb[0]; }
 
+    // Decodes `tile`, which must be the first tile or the previous one + step.
     __device__ __forceinline__ TileInfo decode(int tile) {
         if (tile >= next_begin) {
             while (s + 1 < nphase && tile >= cph[s + 1].tile_begin) ++s;
@@ -133,11 +139,23 @@ struct TileWalker {
             next_begin = s + 1 < nphase ? cph[s + 1].tile_begin : 0x7fffffff;
             pb[0] = cpb[ph.prob_begin];
             if (ph.tiles_per_matrix > pb[0].tiles_per_matrix) pb[1] = cpb[ph.prob_begin + 1];
+            inv_wn[0] = 1.0f / static_cast<float>(pb[0].tiles_n_walk > 0 ? pb[0].tiles_n_walk : 1);
+            inv_wn[1] = 1.0f / static_cast<float>(pb[1].tiles_n_walk > 0 ? pb[1].tiles_n_walk : 1);
+            const int local = tile - ph.tile_begin;
+            lg = local / ph.tiles_per_matrix;
+            lt = local - lg * ph.tiles_per_matrix;
+            sq = step / ph.tiles_per_matrix;
+            sr = step - sq * ph.tiles_per_matrix;
+        } else {
+            lt += sr;
+            lg += sq;
+            if (lt >= ph.tiles_per_matrix) {
+                lt -= ph.tiles_per_matrix;
+                ++lg;
+            }
         }
-        const int local = tile - ph.tile_begin;
-        int g = local / ph.tiles_per_matrix;
-        int t = local - g * ph.tiles_per_matrix;
-        if (ph.reverse) g = G - 1 - g;
+        const int g = ph.reverse ? G - 1 - lg : lg;
+        int t = lt;
         cur = t >= pb[0].tiles_per_matrix ? 1 : 0;
         if (cur) t -= pb[0].tiles_per_matrix;
         const CtlProb& pr = prob();
@@ -148,8 +166,8 @@ struct TileWalker {
         if ((flags & kFlagSym) && TM == BN && !(flags & kFlagShareA)) {
             // Square tiles: row block i holds i + 1 tiles, i (i + 1) / 2 before it.
             i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
-            while (i * (i + 1) / 2 > t) --i;
-            while ((i + 1) * (i + 2) / 2 <= t) ++i;
+            if (i * (i + 1) / 2 > t) --i;
+            if ((i + 1) * (i + 2) / 2 <= t) ++i;
             j = t - i * (i + 1) / 2;
         } else if (flags & kFlagSym) {
             const bool share = flags & kFlagShareA;
@@ -163,8 +181,11 @@ struct TileWalker {
             }
             j = t - acc;
         } else {
-            i = t / pr.tiles_n_walk;
-            j = t - i * pr.tiles_n_walk;
+            const int wn = pr.tiles_n_walk;
+            i = static_cast<int>(static_cast<float>(t) * (cur ? inv_wn[1] : inv_wn[0]));
+            if (i * wn > t) --i;
+            if ((i + 1) * wn <= t) ++i;
+            j = t - i * wn;
         }
         return TileInfo{ph.prob_begin + cur, g, i * TM, j * BN, s};
     }
@@ -294,6 +315,23 @@ __device__ __forceinline__ void merge_upper(uint32_t d, uint32_t dt, int lane) {
     }
 }
 
+// Stores one 16-byte piece v of a staged row at p, clipped to the `left`
+// elements still inside the matrix (the ragged right edge; out of line, it is
+// rare and would otherwise bloat the epilogue's hot code).
+template <int ES>
+static __device__ __noinline__ void store_piece_clipped(uint8_t* p, uint4 v, int left) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (ES == 2) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e < left) reinterpret_cast<uint16_t*>(p)[e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (e < left) reinterpret_cast<uint32_t*>(p)[e] = w[e];
+    }
+}
+
 // Writes a staged block of 32 rows x 64 bytes (64B-swizzled, elements of ES
 // bytes) to rows r0 .. r0 + 31 and the 64 / ES columns from c0 of matrix g
 // of `o`, clipped to rows x cols. Instruction j stores rows 8 j .. 8 j + 7,
@@ -312,21 +350,35 @@ __device__ __forceinline__ void store_rows64(uint32_t stg, const OutView& o, int
         if (gr >= rows || gc >= cols) continue;
         uint8_t* p = static_cast<uint8_t*>(o.p) +
                      (static_cast<long long>(g) * o.stride + static_cast<long long>(gr) * o.ld + gc) * ES;
-        if (gc + EPP <= cols) {
+        if (gc + EPP <= cols)
             *reinterpret_cast<uint4*>(p) = v;
-        } else {
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            if constexpr (ES == 2) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (gc + e < cols)
-                        reinterpret_cast<uint16_t*>(p)[e] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (gc + e < cols) reinterpret_cast<uint32_t*>(p)[e] = w[e];
-            }
-        }
+        else
+            store_piece_clipped<ES>(p, v, cols - gc);
+    }
+}
+
+// The rarer epilogue paths.
+// A 32 x 32 fp32 block, staged and stored as two 16-column halves (inline:
+// the values are a register array, which a call would move to local memory).
+__device__ __forceinline__ void emit_f32(uint32_t slot, const float (&val)[32], const OutView& od, int g, int r0,
+                                             int c0, int M, int N, int lane) {
+    stage_row_f32_half<0>(slot, lane, val);
+    __syncwarp();
+    store_rows64<4>(slot, od, g, r0, c0, M, N, lane);
+    __syncwarp();
+    stage_row_f32_half<1>(slot, lane, val);
+    __syncwarp();
+    store_rows64<4>(slot, od, g, r0, c0 + 16, M, N, lane);
+}
+
+// The transposed copy of a staged fp16 block in sT; for a diagonal block the
+// staged block's upper half is then replaced from it.
+static __device__ __noinline__ void stage_transpose(uint32_t slot, uint32_t sT, bool diag, int lane) {
+    __syncwarp();
+    transpose_block(slot, sT, lane);
+    if (diag) {
+        __syncwarp();
+        merge_upper(slot, sT, lane);
     }
 }
 
@@ -430,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint8_t* sEpi = sB + STAGES * B_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiWarps * SBUF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars(STAGES));
+    const uint32_t pub0 = smem_u32(tmem_slot + 2);  // per-buffer counts of finished epilogue warps
     CtlPhase* cph = reinterpret_cast<CtlPhase*>(tmem_slot + 4);
     CtlProb* cpb = reinterpret_cast<CtlProb*>(cph + kMaxPhases);
 
@@ -466,6 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         mbar_init(drain_bar, 1);
         for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(cbar0 + 8 * b, 1);
+        tmem_slot[2] = 0;
+        tmem_slot[3] = 0;
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < nphase; i += blockDim.x) {
@@ -502,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            TileWalker<BN, CG> walk(cph, cpb, nphase, G);
+            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units * NP);
             for (int w = unit; w < nwalk && ok; w += units) {
                 const TileInfo t = walk.decode(w * NP + pair);
                 const CtlProb& pr = walk.prob();
@@ -592,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             bool ok = true;
             constexpr uint16_t kStageMask = (NP == 2) ? 0xF : 0x3;  // both pairs' CTAs
             const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
-            TileWalker<BN, CG> walk(cph, cpb, nphase, G);
+            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units * NP);
             for (int w = unit; w < nwalk && ok; w += units, ++iter) {
                 const TileInfo t = walk.decode(w * NP + pair);
                 const int pflags = walk.prob().flags;
@@ -769,23 +824,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     // read it back.
                     auto emit = [&](const float (&val)[32], const OutView& od, const OutView& odt) {
                         if (f32) {
-                            stage_row_f32_half<0>(slot, lane, val);
-                            __syncwarp();
-                            store_rows64<4>(slot, od, t.g, r0, c0, M, N, lane);
-                            __syncwarp();
-                            stage_row_f32_half<1>(slot, lane, val);
-                            __syncwarp();
-                            store_rows64<4>(slot, od, t.g, r0, c0 + 16, M, N, lane);
+                            emit_f32(slot, val, od, t.g, r0, c0, M, N, lane);
                         } else {
                             stage_row_f16(slot, lane, val);
-                            if (mirror || diag_block) {
-                                __syncwarp();
-                                transpose_block(slot, sT, lane);
-                                if (diag_block) {
-                                    __syncwarp();
-                                    merge_upper(slot, sT, lane);
-                                }
-                            }
+                            if (mirror || diag_block) stage_transpose(slot, sT, diag_block, lane);
                             __syncwarp();
                             store_rows64<2>(slot, od, t.g, r0, c0, M, N, lane);
                             if (mirror) store_rows64<2>(sT, odt, t.g, c0, r0, N, M, lane);
@@ -811,14 +853,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
+                // Publish the tile once per CTA: each warp counts itself done
+                // (a CTA-scope release covering its lanes' stores, which the
+                // warp barrier above ordered before it); the warp that
+                // completes the count releases the CTA's part of the tile to
+                // the matrix's counter, cumulatively over all eight warps'
+                // stores, so only one warp per tile waits for its stores to
+                // land. The count comes before the accumulator is handed
+                // back, so a buffer's counts never mix two tiles.
+                const uint32_t old = atom_add_acqrel_cta(pub0 + 4 * buf, 1);
                 if constexpr (CG == 1)
                     mbar_arrive(acce0 + 8 * buf);
                 else
                     mbar_arrive_cluster(acce_lead + 8 * buf);
-                // Publish this warp's part of the tile: the release is
-                // cumulative over the lanes' stores, which the warp barrier
-                // above ordered before it.
-                if (P.counters) red_release_add(P.counters + t.g, 1);
+                if (P.counters && old % kEpiWarps == kEpiWarps - 1) red_release_add(P.counters + t.g, kEpiWarps);
             }
         }
         // C loads still in flight (only after a failed wait) land before exit.

@@ -338,6 +338,13 @@ __device__ __forceinline__ int ld_acquire(const int* addr) {
     return v;
 }
 
+// Shared-memory fetch-and-add with acquire-release semantics at CTA scope.
+__device__ __forceinline__ uint32_t atom_add_acqrel_cta(uint32_t smem_addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr), "r"(v) : "memory");
+    return old;
+}
+
 // A relaxed read of a counter: issued early, its value is used later; a
 // value that shows the wanted count is turned into an acquire by
 // fence_acq_rel() (relaxed read, then fence: the acquire pattern of the PTX
