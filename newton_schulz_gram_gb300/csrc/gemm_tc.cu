@@ -28,7 +28,8 @@
 // result is exactly symmetric.
 //
 // Transposed sub-blocks are built in shared memory with ldmatrix.trans /
-// stmatrix; fp16 staging uses a 64-byte swizzle, fp32 staging a 128-byte one.
+// stmatrix; all staging uses 64-byte rows with the 64-byte swizzle (fp32 blocks
+// are staged as two 16-column halves).
 #include <cstdio>
 
 #include "gemm.cuh"

@@ -345,20 +345,6 @@ __device__ __forceinline__ uint32_t atom_add_acqrel_cta(uint32_t smem_addr, uint
     return old;
 }
 
-// A relaxed read of a counter: issued early, its value is used later; a
-// value that shows the wanted count is turned into an acquire by
-// fence_acq_rel() (relaxed read, then fence: the acquire pattern of the PTX
-// memory model).
-__device__ __forceinline__ int ld_relaxed(const int* addr) {
-    int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void fence_acq_rel() {
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
 // Spins until *addr >= target (acquire). Bounded like the mbarrier waits.
 static __device__ __noinline__ bool wait_counter(const int* addr, int target, int* err) {
     if (ld_acquire(addr) >= target) return true;
