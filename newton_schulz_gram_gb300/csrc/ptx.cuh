@@ -66,9 +66,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Bounded.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The bounded spin of mbar_wait, out of line.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int* err) {
     const uint64_t t0 = globaltimer();
     while (true) {
         for (int i = 0; i < 64; ++i)
@@ -79,6 +78,13 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int
             return false;
         }
     }
+}
+
+// Waits for the phase with the given parity to complete. Bounded. The first
+// test is inline: on the issue paths the phase is usually complete already,
+// and a call per k-block costs the single issuing thread measurable time.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, err);
 }
 
 // -------------------------------------------------------------------- TMA
