@@ -649,16 +649,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             constexpr uint16_t kStageMask = (NP == 2) ? 0xF : 0x3;  // both pairs' CTAs
             const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
             TileWalker<BN, CG> walk(cph, cpb, nphase, G, units * NP);
+            // Stage-0 descriptors of both operand layouts; a stage adds its
+            // byte offset / 16 to the start-address field (addresses < 256 KB).
+            const uint64_t ak0 = sw128_kmajor_desc(smem_u32(sA)), amn0 = sw128_mnmajor_desc(smem_u32(sA), kMnBlockBytes);
+            const uint64_t bk0 = sw128_kmajor_desc(smem_u32(sB)), bmn0 = sw128_mnmajor_desc(smem_u32(sB), kMnBlockBytes);
             for (int w = unit; w < nwalk && ok; w += units, ++iter) {
                 const TileInfo t = walk.decode(w * NP + pair);
                 const int pflags = walk.prob().flags;
                 const int kblocks = (walk.prob().K + BK - 1) / BK;
                 const int buf = iter & 1;
-                const bool a_mn0 = pflags & kFlagAmn;
-                const bool b_mn0 = pflags & kFlagBmn;
-                const bool a_sym = pflags & kFlagAsym;
-                const bool b_sym = pflags & kFlagBsym;
-                const int ti = t.m0 / TM, tj = t.n0 / TM;
+                // First k-block read transposed (lower-only operands: the
+                // k-blocks right of the diagonal tile); MN-major operands are
+                // transposed from the first k-block on.
+                const int a_tkb = (pflags & kFlagAmn) ? 0 : (pflags & kFlagAsym) ? (t.m0 + TM) / BK : 0x7fffffff;
+                const int b_tkb = (pflags & kFlagBmn) ? 0 : (pflags & kFlagBsym) ? (t.n0 + TM) / BK : 0x7fffffff;
                 if (!mbar_wait(acce0 + 8 * buf, ((iter >> 1) & 1) ^ 1, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
@@ -669,18 +673,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                     tc_fence_after();
                     // The operand layouts the producer chose for this k-block.
-                    const int kt = (kb * BK) / TM;
-                    const uint32_t a_mn = (a_mn0 || (a_sym && kt > ti)) ? 1u : 0u;
-                    const uint32_t b_mn = (b_mn0 || (b_sym && kt > tj)) ? 1u : 0u;
-                    const uint32_t idesc = IDESC | (a_mn << 15) | (b_mn << 16);
+                    const bool a_mn = kb >= a_tkb, b_mn = kb >= b_tkb;
+                    const uint32_t idesc = IDESC | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
                     // Per 16-wide k step: 32 bytes along a K-major row, or two
                     // 8-row groups (2048 bytes) of an MN-major tile.
                     const uint32_t a_step = a_mn ? (2048 >> 4) : (32 >> 4);
                     const uint32_t b_step = b_mn ? (2048 >> 4) : (32 >> 4);
-                    const uint32_t sa = smem_u32(sA + stage * A_BYTES);
-                    const uint32_t sb = smem_u32(sB + stage * B_BYTES);
-                    const uint64_t adesc = a_mn ? sw128_mnmajor_desc(sa, kMnBlockBytes) : sw128_kmajor_desc(sa);
-                    const uint64_t bdesc = b_mn ? sw128_mnmajor_desc(sb, kMnBlockBytes) : sw128_kmajor_desc(sb);
+                    const uint64_t adesc = (a_mn ? amn0 : ak0) + ((stage * A_BYTES) >> 4);
+                    const uint64_t bdesc = (b_mn ? bmn0 : bk0) + ((stage * B_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         tc_mma_f16<CG>(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc,
