@@ -292,12 +292,12 @@ __device__ __forceinline__ void stage_row_f32_half(uint32_t base, int lane, cons
 // dst = src^T for a 32 x 32 fp16 block (both 64B-swizzled): 8 x 8 block (R, i)
 // of src, loaded transposed, is stored as block (i, R) of dst.
 __device__ __forceinline__ void transpose_block(uint32_t src, uint32_t dst, int lane) {
+    uint32_t a[4][4];  // all loads first, then all stores (one round trip, not four)
 #pragma unroll
-    for (int R = 0; R < 4; ++R) {
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(sw64_addr(src, 8 * R + (lane & 7), 8 * (lane >> 3)), a0, a1, a2, a3);
-        stmatrix_x4(sw64_addr(dst, lane, 8 * R), a0, a1, a2, a3);
-    }
+    for (int R = 0; R < 4; ++R)
+        ldmatrix_x4_trans(sw64_addr(src, 8 * R + (lane & 7), 8 * (lane >> 3)), a[R][0], a[R][1], a[R][2], a[R][3]);
+#pragma unroll
+    for (int R = 0; R < 4; ++R) stmatrix_x4(sw64_addr(dst, lane, 8 * R), a[R][0], a[R][1], a[R][2], a[R][3]);
 }
 
 // Diagonal block: row `lane` keeps its lower part (col <= lane) and takes the
@@ -343,10 +343,15 @@ __device__ __forceinline__ void store_rows64(uint32_t stg, const OutView& o, int
     constexpr int EPP = 16 / ES;  // elements per 16-byte piece
     const int k = lane & 3;
     const int gc = c0 + EPP * k;
+    // All four shared-memory reads first: under load each round trip costs
+    // hundreds of cycles, so they are issued back to back, not one per store.
+    uint4 vv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) vv[j] = ld_shared_v4(sw64_piece(stg, 8 * j + (lane >> 2), k));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int r = 8 * j + (lane >> 2);
-        const uint4 v = ld_shared_v4(sw64_piece(stg, r, k));
+        const uint4 v = vv[j];
         const int gr = r0 + r;
         if (gr >= rows || gc >= cols) continue;
         uint8_t* p = static_cast<uint8_t*>(o.p) +
