@@ -166,3 +166,25 @@ def test_restart_schedule_entry_point(gns):
             assert_parity(out[g], O.gram_ns(X[g].astype(np.float64), 5, None, list(restarts)), what=str(restarts))
     with pytest.raises(Exception):
         gns.gns_orthogonalize_batched_schedule(torch.from_numpy(X.copy()).cuda(), 5, (5,))
+
+
+# Every tile configuration of the GEMM program, forced through GNS_TILE (the
+# library picks one by n otherwise): single-CTA 128 x 128 and 128 x 256 tiles,
+# CTA pairs, and two pairs per cluster sharing A by balanced multicast, also
+# for the symmetric products (GNS_SHARE_SYM=1, rows padded to even tile
+# counts). Ragged rectangular and square buckets, so the clipped stores, the
+# fp32 output with an addend (last standard-NS step) and the lower-only reads
+# all run in each configuration.
+TILE_CONFIGS = [("128x1", "0"), ("256x1", "0"), ("256x2", "0"), ("256x2x2", "0"), ("256x2x2", "1")]
+
+
+@pytest.mark.parametrize("tile,share_sym", TILE_CONFIGS)
+@pytest.mark.parametrize("G,R,C", [(2, 520, 1100), (2, 1100, 520), (2, 384, 384)])
+def test_forced_tile_configs_match_oracle(gns, monkeypatch, tile, share_sym, G, R, C):
+    monkeypatch.setenv("GNS_TILE", tile)
+    monkeypatch.setenv("GNS_SHARE_SYM", share_sym)
+    X = gen.gaussian_bucket(G, R, C, seed=700 + R + C)
+    out = run_gpu(gns, X)
+    for g in range(G):
+        ref = O.orthogonalize(X[g].astype(np.float64))
+        assert_parity(out[g], ref, what=f"{tile}/{share_sym} {R}x{C}[{g}]")
