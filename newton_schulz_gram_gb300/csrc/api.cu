@@ -1135,7 +1135,31 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
         if (std::atoll(e) > 0) chunk_bytes = std::atoll(e) << 20;
     }
     const int gc = static_cast<int>(std::max(1LL, std::min<long long>(G, chunk_bytes / (per * 4))));
-    const int nchunks = (G + gc - 1) / gc;
+    // The first chunk's copy in and the last chunk's orthogonalization and
+    // copy out overlap nothing, so those two chunks are half size; the link
+    // (not the GPU) bounds the rest.
+    std::vector<int> sizes;
+    {
+        int rem = G;
+        if (G > 2 * gc && gc > 1) {
+            const int h = gc / 2;
+            sizes.push_back(h);
+            rem -= 2 * h;
+            while (rem > 0) {
+                const int n = std::min(gc, rem);
+                sizes.push_back(n);
+                rem -= n;
+            }
+            sizes.push_back(h);
+        } else {
+            while (rem > 0) {
+                const int n = std::min(gc, rem);
+                sizes.push_back(n);
+                rem -= n;
+            }
+        }
+    }
+    const int nchunks = static_cast<int>(sizes.size());
     std::vector<cudaEvent_t> ev(2 * static_cast<size_t>(nchunks) + 1, nullptr);
     int rc = GNS_OK;
     auto cleanup = [&]() {
@@ -1154,8 +1178,9 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
         // The copies start after the caller's earlier work on its stream.
         CK(cudaEventRecord(ev[0], s));
         CK(cudaStreamWaitEvent(st->h2d, ev[0], 0));
-        for (int c = 0; c < nchunks; ++c) {
-            const int g0 = c * gc, n = std::min(gc, G - g0);
+        int g0 = 0;
+        for (int c = 0; c < nchunks; g0 += sizes[c], ++c) {
+            const int n = sizes[c];
             float* dev = st->stage + static_cast<long long>(g0) * per;
             float* host = host_ptr + static_cast<long long>(g0) * per;
             const size_t b = static_cast<size_t>(n) * per * sizeof(float);
