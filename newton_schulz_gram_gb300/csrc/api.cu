@@ -266,6 +266,13 @@ TileShape choose_tile(int n) {
     return n >= 3072 ? TileShape{256, 2, 2} : TileShape{256, 2, 1};
 }
 
+// Non-symmetric products walk their tiles column by column unless
+// GNS_COL_WALK=0 (row by row).
+bool col_walk() {
+    const char* e = std::getenv("GNS_COL_WALK");
+    return !(e && std::atoi(e) == 0);
+}
+
 bool share_symmetric() {
     const char* e = std::getenv("GNS_SHARE_SYM");
     return e && std::atoi(e) != 0;
@@ -405,6 +412,7 @@ class ProgramBuilder {
         if (sp.lower) flags |= kFlagLower;
         if (sp.muon) flags |= kFlagMuon;
         if (share) flags |= kFlagShareA;
+        if (!sp.sym && !share && col_walk()) flags |= kFlagColWalk;
         if (sp.C) {
             flags |= kFlagC;
             pr.C = static_cast<const __half*>(sp.C->p);
@@ -431,6 +439,7 @@ class ProgramBuilder {
         pr.N = N;
         pr.K = Ka;
         pr.tiles_n = (pr.N + bn - 1) / bn;
+        pr.tiles_m = (pr.M + 128 * cg - 1) / (128 * cg);
         pr.tiles_per_matrix = gemm_tiles_per_matrix(pr.M, pr.N, bn, cg, sp.sym, ts_.np, share, &pr.tiles_n_walk);
         pr.flags = flags;
         return GNS_OK;

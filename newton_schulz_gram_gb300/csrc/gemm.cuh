@@ -44,7 +44,11 @@ enum GemmFlags : int {
     // acc) updates the bf16 weight of the same (row, column) of matrix g,
     // W <- SR_bf16((1 - lr wd) W - (lr scale) o), with the stochastic
     // rounding counter of global index w_base[g] + row N + column.
-    kFlagMuon = 2048
+    kFlagMuon = 2048,
+    // Non-symmetric product walked column by column: the tiles sharing a B
+    // column block run together, so B (for Q X, the large X) is read from
+    // DRAM about once and hits L2 for the other tile rows.
+    kFlagColWalk = 4096
 };
 
 // Parameters of the fused Muon update (kFlagMuon).
@@ -76,6 +80,7 @@ struct GemmProblem {
     int M, N, K;
     int tiles_n;           // tile columns of the matrix
     int tiles_n_walk;      // tile columns enumerated per row (tiles_n, or even with kFlagShareA)
+    int tiles_m;           // tile rows of the matrix
     int tiles_per_matrix;  // tiles enumerated per matrix (even when pairs share a cluster)
     int flags;
     // Indices into GemmProgram::maps (-1 when unused). K-major operand maps:

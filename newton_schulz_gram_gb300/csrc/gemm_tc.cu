@@ -79,7 +79,7 @@ struct CtlPhase {
     int tile_begin, tiles_per_matrix, prob_begin, reverse, wait_tiles;
 };
 struct CtlProb {
-    int tiles_per_matrix, tiles_n, tiles_n_walk, flags, K;
+    int tiles_per_matrix, tiles_n, tiles_n_walk, flags, K, tiles_m;
     int mA, mB, mAt, mBt, mC;
 };
 constexpr int kCtlBytes = kMaxPhases * static_cast<int>(sizeof(CtlPhase)) + kMaxProblems * static_cast<int>(sizeof(CtlProb));
@@ -122,7 +122,7 @@ struct TileWalker {
     int s = -1, next_begin = 0;  // current phase and the first tile of the next one
     CtlPhase ph{};
     CtlProb pb[2]{};             // the phase's problems
-    float inv_wn[2]{};           // 1 / tiles_n_walk of each problem
+    float inv_wn[2]{};           // 1 / (tiles walked per row, or per column) of each problem
     int lg = 0, lt = 0;          // position of the last tile: matrix slot, tile within the matrix
     int sq = 0, sr = 0;          // step = sq tiles_per_matrix + sr
     int cur = 0;                 // which of pb[] the last decoded tile belongs to
@@ -140,8 +140,10 @@ struct TileWalker {
             next_begin = s + 1 < nphase ? cph[s + 1].tile_begin : 0x7fffffff;
             pb[0] = cpb[ph.prob_begin];
             if (ph.tiles_per_matrix > pb[0].tiles_per_matrix) pb[1] = cpb[ph.prob_begin + 1];
-            inv_wn[0] = 1.0f / static_cast<float>(pb[0].tiles_n_walk > 0 ? pb[0].tiles_n_walk : 1);
-            inv_wn[1] = 1.0f / static_cast<float>(pb[1].tiles_n_walk > 0 ? pb[1].tiles_n_walk : 1);
+            for (int q = 0; q < 2; ++q) {
+                const int w = (pb[q].flags & kFlagColWalk) ? pb[q].tiles_m : pb[q].tiles_n_walk;
+                inv_wn[q] = 1.0f / static_cast<float>(w > 0 ? w : 1);
+            }
             const int local = tile - ph.tile_begin;
             lg = local / ph.tiles_per_matrix;
             lt = local - lg * ph.tiles_per_matrix;
@@ -181,6 +183,12 @@ struct TileWalker {
                 ++i;
             }
             j = t - acc;
+        } else if (flags & kFlagColWalk) {
+            const int wm = pr.tiles_m;
+            j = static_cast<int>(static_cast<float>(t) * (cur ? inv_wn[1] : inv_wn[0]));
+            if (j * wm > t) --j;
+            if ((j + 1) * wm <= t) ++j;
+            i = t - j * wm;
         } else {
             const int wn = pr.tiles_n_walk;
             i = static_cast<int>(static_cast<float>(t) * (cur ? inv_wn[1] : inv_wn[0]));
@@ -228,6 +236,10 @@ __device__ __forceinline__ TileInfo decode_tile(const CtlPhase* cph, const CtlPr
             ++i;
         }
         j = t - acc;
+    } else if (flags & kFlagColWalk) {
+        const int wm = cpb[p].tiles_m;
+        j = t / wm;
+        i = t - j * wm;
     } else {
         const int wn = cpb[p].tiles_n_walk;
         i = t / wn;
@@ -535,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     for (int i = threadIdx.x; i < P.nprob; i += blockDim.x) {
         const GemmProblem& pr = P.prob[i];
-        cpb[i] = CtlProb{pr.tiles_per_matrix, pr.tiles_n, pr.tiles_n_walk, pr.flags, pr.K,
+        cpb[i] = CtlProb{pr.tiles_per_matrix, pr.tiles_n, pr.tiles_n_walk, pr.flags, pr.K, pr.tiles_m,
                          pr.mA, pr.mB, pr.mAt, pr.mBt, pr.mC};
     }
     if (warp == 0 && lane == 0) {
