@@ -251,7 +251,7 @@ struct TileShape {
     int bn, cg, np;
 };
 
-TileShape choose_tile(int n) {
+TileShape choose_tile(int n, int G, int num_sms) {
     const char* force = std::getenv("GNS_TILE");
     if (force) {
         const std::string f(force);
@@ -261,6 +261,14 @@ TileShape choose_tile(int n) {
         if (f == "256x2x2") return {256, 2, 2};
     }
     if (n < 192) return {128, 1, 1};
+    // A bucket whose n x n products give the CTA pairs less than about one and
+    // a half waves of 256 x 256 tiles leaves pairs idle: single-CTA 128 x 128
+    // tiles quadruple the tile count (measured: 16 x 256 x 4096, 32 x 384 x 1536
+    // and 8 x 512 x 2048 run 15-17 % faster that way, 24 x 1024 x 4096 and
+    // 256 x 512 x 2048 slower).
+    const long long t2 = (n + 255) / 256;
+    const long long pair_tiles = static_cast<long long>(G) * t2 * (t2 + 1) / 2;
+    if (2 * pair_tiles < 3LL * (num_sms / 2)) return {128, 1, 1};
     // Two pairs per cluster (A shared) pay off only for large matrices: the
     // 4-CTA clusters leave 8 of the 152 SMs idle.
     return n >= 3072 ? TileShape{256, 2, 2} : TileShape{256, 2, 1};
@@ -583,7 +591,7 @@ Mat mat16(char* ws, size_t off, int rows, int cols, long long ld) {
 int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in,
              const MatrixSet* grads, float mu, int steps, uint64_t restarts, const Coeffs& cf, const OutSpec& os,
              cudaStream_t s) {
-    const TileShape ts = choose_tile(g.n);
+    const TileShape ts = choose_tile(g.n, Gc, st.num_sms);
     ProgramBuilder prog(st, Gc, ts, reinterpret_cast<int*>(st.ws + L.counters), s);
     char* ws = st.ws;
     // Symmetric n x n intermediates are stored lower-only (diagonal tiles in
@@ -1283,7 +1291,7 @@ int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, i
     p.beta = C ? beta : 0.0f;
     p.sym = true;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    ProgramBuilder prog(*st, G, choose_tile(n), nullptr, s);
+    ProgramBuilder prog(*st, G, choose_tile(n, G, st->num_sms), nullptr, s);
     RET(prog.phase(p, nullptr, false));
     return prog.flush();
 }
