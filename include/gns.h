@@ -88,7 +88,10 @@ int gns_orthogonalize_batched_schedule(float* ptr, int G, int R, int C, int step
  * host_ptr is fp32 [G][R][C] in host memory (pinned memory gives full copy
  * speed); the library copies it to a device staging buffer it owns, runs
  * gns_orthogonalize_batched there, copies the result back and synchronizes
- * `stream` before returning.
+ * `stream` before returning. The bucket is pipelined in chunks of about
+ * 64 MiB (GNS_HOST_CHUNK_MB overrides), the first and last half size: chunk
+ * copies in and out run on two library-owned streams and overlap the
+ * neighbouring chunks' orthogonalization on `stream`.
  */
 int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int steps,
                                    int restart_at, const float* coeffs, void* stream);
