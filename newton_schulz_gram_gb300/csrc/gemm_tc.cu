@@ -787,8 +787,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             }
 
-            int okw = mbar_wait(accf0 + 8 * buf, (iter >> 1) & 1, err) ? 1 : 0;
-            if (!okw) break;
+            // Every lane waits; the warp goes on only if all saw the phase (a lane
+            // that gave up on the bounded wait takes the warp out with it, so the
+            // warp-wide tcgen05.ld below never runs divergent).
+            if (!__all_sync(0xffffffffu, mbar_wait(accf0 + 8 * buf, (iter >> 1) & 1, err))) break;
             tc_fence_after();
 
             uint32_t m = am;
@@ -803,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c * 32, acc);
                 uint4 cb[4];
                 if (hasC) {
-                    if (!mbar_wait(cbw + 8 * (k & 1), (cpar >> (k & 1)) & 1, err)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(cbw + 8 * (k & 1), (cpar >> (k & 1)) & 1, err))) {
                         ok = false;
                         break;
                     }
