@@ -76,21 +76,48 @@ def gemm_source_hash():
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_tc_mlp_bucket_24x1024x4096.traffic.txt")
+
+
 def profiled_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "gemm_tc_mlp_bucket_24x1024x4096.md")
+    """DRAM bytes per GEMM launch of the 24-matrix bucket from the committed
+    summary that --record-traffic wrote from an ncu capture, if that capture
+    was taken on the current kernel source (else None)."""
     try:
-        text = open(path).read()
+        text = open(TRAFFIC_FILE).read()
     except OSError:
         return None
-    src = gemm_source_hash()
-    for line in text.splitlines():
-        if line.startswith("traffic_bytes_per_launch:"):
-            parts = dict(kv.split("=") for kv in line.split(":", 1)[1].split())
-            if parts.get("source_hash") == src:
-                return float(parts["bytes"])
-    return None
+    kv = dict(tok.split("=", 1) for tok in text.split() if "=" in tok)
+    if kv.get("source_hash") != gemm_source_hash():
+        return None
+    return float(kv["bytes_per_launch"])
+
+
+def record_traffic(csv_path, matrices):
+    """Reads an `ncu --csv --page raw` capture of gemm_tc launches (metrics
+    dram__bytes_read.sum and dram__bytes_write.sum, bytes) and writes the
+    traffic summary the bench reads: the mean per launch, scaled from the
+    captured bucket of `matrices` matrices to the benchmark's 24 (the
+    per-matrix traffic does not depend on the bucket size)."""
+    import csv
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(line for line in f if not line.startswith("=="))]
+    hdr = rows[0]
+    ki, ri, wi = hdr.index("Kernel Name"), hdr.index("dram__bytes_read.sum"), hdr.index("dram__bytes_write.sum")
+    units = rows[1]
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    vals = []
+    for r in rows[2:]:
+        if "gemm_tc" in r[ki]:
+            vals.append(float(r[ri].replace(",", "")) * scale[units[ri]] + float(r[wi].replace(",", "")) * scale[units[wi]])
+    if not vals:
+        raise SystemExit("no gemm_tc launch in the capture")
+    per = sum(vals) / len(vals) * 24.0 / matrices
+    with open(TRAFFIC_FILE, "w") as f:
+        f.write(f"kernel=gemm_tc source_hash={gemm_source_hash()} launches_captured={len(vals)} "
+                f"matrices_captured={matrices} bytes_per_captured_launch={sum(vals) / len(vals):.0f} "
+                f"bytes_per_launch={per:.0f}\n")
+    print(open(TRAFFIC_FILE).read().strip())
 
 
 class ClockSampler:
@@ -108,7 +135,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -239,17 +266,161 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def median(v):
+    return statistics.median(v) if v else None
+
+
+def quantiles(v):
+    """(min, p25, median, p75, max) of a list of numbers."""
+    s = sorted(v)
+    if not s:
+        return None
+    q = statistics.quantiles(s, n=4, method="inclusive") if len(s) > 1 else [s[0]] * 3
+    return [s[0], q[0], q[1], q[2], s[-1]]
+
+
+def time_calls(torch, stream, fn, calls, warmup=2, blocks=5):
+    """Median ms per call over `blocks` blocks of `calls` calls each (CUDA
+    events on the launching stream, synchronized on both sides)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    per_call = []
+    for _ in range(blocks):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(calls):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per_call.append(a.elapsed_time(b) / calls)
+    return median(per_call), quantiles(per_call)
+
+
+def bucket_line(gns, torch, stream, dev, name, G_, R_, C_, calls, peak):
+    """Throughput of one bucket shape (inputs N(0, 1) drawn on the device: the
+    work does not depend on the values)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    x = torch.randn(G_, R_, C_, device=dev, generator=gen)
+    l0 = gns.gns_launch_count()
+    gns.gns_orthogonalize_batched(x, T_STEPS, RESTART)
+    torch.cuda.synchronize()
+    launches = gns.gns_launch_count() - l0
+    ms, q = time_calls(torch, stream, lambda: gns.gns_orthogonalize_batched(x, T_STEPS, RESTART), calls)
+    if gns.gns_get_status() != 0:
+        raise SystemExit(f"device status error in {name}")
+    n, m = min(R_, C_), max(R_, C_)
+    alg = G_ * alg_flops_per_matrix(n, m)
+    tf = alg / (ms / 1e3) / 1e12
+    del x
+    return {"workload": name, "G": G_, "R": R_, "C": C_, "ms_per_call": ms, "ms_quartiles": q,
+            "matrices_per_s": G_ / (ms / 1e3), "algorithmic_tflops": tf, "frac_of_peak": tf / peak,
+            "effective_tflops": G_ * eff_flops_per_matrix(n, m) / (ms / 1e3) / 1e12,
+            "launches_per_call": launches}
+
+
+def llama7b_line(gns, torch, stream, dev, peaks):
+    """One Muon step over the 7B Llama-like stack (Dion3 Fig. 1 workload;
+    W bf16 N(0, 0.02), G bf16 N(0, 1e-3), M fp32, drawn on the device), and
+    the standalone update kernel's HBM rate."""
+    from inputs import generators as gen_mod
+    shapes = gen_mod.llama7b_shapes()
+    g = torch.Generator(device=dev)
+    g.manual_seed(5000)
+    W, Gr, M = [], [], []
+    for _, r, c in shapes:
+        W.append((0.02 * torch.randn(r, c, device=dev, generator=g)).to(torch.bfloat16))
+        Gr.append((1e-3 * torch.randn(r, c, device=dev, generator=g)).to(torch.bfloat16))
+        M.append(1e-3 * torch.randn(r, c, device=dev, generator=g))
+    params = sum(w.numel() for w in W)
+    alg = 0
+    for _, r, c in shapes:
+        n, m = min(r, c), max(r, c)
+        alg += 4 * T_STEPS * n ** 3 if n == m else alg_flops_per_matrix(n, m)
+    step = [2]
+
+    def one():
+        gns.muon_step(W, Gr, M, lr=0.02, wd=0.01, mu=0.95, seed=0, step=step[0])
+        step[0] += 1
+
+    one()
+    torch.cuda.synchronize()
+    gns.gns_profile_enable(True)
+    gns.gns_profile_read()
+    ms, q = time_calls(torch, stream, one, calls=1, warmup=0, blocks=3)
+    gns.gns_profile_enable(False)
+    prof = gns.gns_profile_read()
+    if gns.gns_get_status() != 0:
+        raise SystemExit("device status error in the 7B step")
+    nc_n, nc_ms = prof["norm_cast"]
+    # Momentum + norm + cast over the 3 timed steps: M read and written (8 B),
+    # G read (2 B), fp16 X written (2 B) per parameter.
+    nc_step_ms = nc_ms / 3
+    nc_gbs = 12.0 * params / (nc_step_ms / 1e3) / 1e9 if nc_ms > 0 else None
+    del W, Gr, M
+    torch.cuda.empty_cache()
+    # The standalone update kernel (W <- SR_bf16(decay W - step O)) over 2^30
+    # elements: W read and written, O read, 6 B per element.
+    N = 1 << 30
+    w = torch.zeros(N, dtype=torch.bfloat16, device=dev).view(32768, 32768)
+    o = torch.zeros(N, dtype=torch.float16, device=dev).view(32768, 32768)
+    ums, uq = time_calls(torch, stream, lambda: gns.gns_muon_update(w, o, 0.02, 0.01, 1.0, 0, 1), calls=1,
+                         warmup=2, blocks=10)
+    del w, o
+    torch.cuda.empty_cache()
+    upd_gbs = 6.0 * N / (ums / 1e3) / 1e9
+    return {"workload": "llama7b_muon_step (224 matrices, 6.98e9 params, buckets by shape)",
+            "ms_per_step": ms, "ms_quartiles": q, "params": params, "algorithmic_tflops": alg / (ms / 1e3) / 1e12,
+            "frac_of_peak": alg / (ms / 1e3) / 1e12 / peaks["tflops_sustained"],
+            "peak_used": "sustained bf16 (a step of about 0.3 s)",
+            "elementwise": {
+                "norm_cast_momentum": {"ms_per_step": nc_step_ms, "launches_per_step": nc_n / 3, "gbs": nc_gbs,
+                                       "bytes_per_element": 12, "frac_of_hbm": (nc_gbs / peaks["hbm_gbs"]) if nc_gbs else None},
+                "muon_update_kernel": {"elements": N, "ms": ums, "ms_quartiles": uq, "gbs": upd_gbs,
+                                       "bytes_per_element": 6, "frac_of_hbm": upd_gbs / peaks["hbm_gbs"]}}}
+
+
+def single_thread_oracle(budget_s=10.0):
+    """The oracle on one host thread (BLAS threads pinned to 1 in a child
+    process), over matrices of the benchmark bucket until the budget is spent."""
+    code = ("import sys, time, numpy as np; sys.path.insert(0, %r); from inputs import generators as gen; "
+            "from oracle import gram_ns; X = gen.gaussian_bucket(3, %d, %d, %d); t0 = time.perf_counter(); n = 0\n"
+            "while n < 3:\n"
+            "    gram_ns.orthogonalize(X[n].astype(np.float64), %d, None, %d); n += 1\n"
+            "    if time.perf_counter() - t0 > %f: break\n"
+            "print(n, time.perf_counter() - t0)") % (ROOT, R, C, rank_seed(0), T_STEPS, RESTART, budget_s)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=budget_s * 6 + 60)
+        n, dt = r.stdout.split()[-2:]
+        n, dt = int(n), float(dt)
+    except Exception as e:  # reported, not fatal
+        return {"error": str(e)[:200]}
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} {R}x{C} matrices of the bucket, fp64 numpy, one thread, {dt:.1f} s"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gns", choices=["gns", "reference"])
+    ap.add_argument("--min-timed-s", type=float, default=1.5,
+                    help="repeat the timed block of K steps (at least 5 times) until this much time is timed")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' table")
     ap.add_argument("--G", type=int, default=24, help="matrices per bucket (24 is the benchmark; smaller only for profiling)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="write the GEMM traffic summary from an ncu --csv --page raw capture and exit")
+    ap.add_argument("--traffic-matrices", type=int, default=12, help="matrices in the captured launch")
     args = ap.parse_args()
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, args.traffic_matrices)
     global G
     G = args.G
     if args.warmup < 3:
@@ -283,36 +454,45 @@ def main():
         if dist is not None:
             dist.barrier()
 
-    sampler = ClockSampler(smi_id(torch, local))
-    sampler.start()
     for _ in range(args.warmup):
         gns.gns_orthogonalize_batched(x, T_STEPS, RESTART)
     if gns.gns_get_status() != 0:
         raise SystemExit("device status error during warm-up")
 
-    # Timed region: K steps, CUDA events on the launching stream.
-    barrier()
-    launches0 = gns.gns_launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        gns.gns_orthogonalize_batched(x, T_STEPS, RESTART)
-    e1.record(stream)
-    barrier()
-    launches = gns.gns_launch_count() - launches0
-    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    # Timed region: blocks of exactly K steps, each bracketed by a barrier and
+    # a synchronization and timed with CUDA events on the launching stream;
+    # at least 5 blocks, more until --min-timed-s is covered. The clocks are
+    # sampled throughout.
+    sampler = ClockSampler(smi_id(torch, local))
+    sampler.start()
+    time.sleep(0.3)
+    block_ms, launches = [], 0
+    while len(block_ms) < 5 or (sum(block_ms) < 1e3 * args.min_timed_s and len(block_ms) < 500):
+        barrier()
+        l0 = gns.gns_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            gns.gns_orthogonalize_batched(x, T_STEPS, RESTART)
+        e1.record(stream)
+        barrier()
+        launches = gns.gns_launch_count() - l0
+        block_ms.append(max_over_ranks(e0.elapsed_time(e1), dist, dev))
+    sampler.stop()
+    status = gns.gns_get_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed region")
+    ms = median(block_ms)
+    step_q = [b / args.steps for b in quantiles(block_ms)]
 
-    # Same K steps again with per-launch events, for the per-kernel roofline.
+    # One more block with per-launch events, for the per-kernel roofline.
     gns.gns_profile_enable(True)
+    gns.gns_profile_read()
     for _ in range(args.steps):
         gns.gns_orthogonalize_batched(x, T_STEPS, RESTART)
     torch.cuda.synchronize(dev)
     gns.gns_profile_enable(False)
     prof = gns.gns_profile_read()
-    sampler.stop()
-    status = gns.gns_get_status()
-    if status != 0:
-        raise SystemExit(f"device status {status} after the timed region")
 
     # End to end through the host-buffer entry point.
     e2e_steps = max(1, args.e2e_steps)
@@ -326,20 +506,22 @@ def main():
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
 
     peaks = load_peaks()
-    value = job_throughput(G * args.steps, world, ms / 1e3)
     per_step_s = ms / 1e3 / args.steps
+    value = job_throughput(G, world, per_step_s)
     alg = G * alg_flops_per_matrix(R, C)
     eff = G * eff_flops_per_matrix(R, C)
     gemm_n, gemm_ms = prof["gemm_tc"]
-    gemm_launches_per_step = gemm_n / args.steps
     achieved = (alg * args.steps) / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
-    traffic = profiled_traffic()
-    kernels = {k: {"launches": n, "total_ms": round(t, 4), "share": round(t / max(1e-9, sum(v[1] for v in prof.values())), 4)}
+    total_prof = max(1e-9, sum(v[1] for v in prof.values()))
+    kernels = {k: {"launches": n, "total_ms": round(t, 4), "share": round(t / total_prof, 4)}
                for k, (n, t) in prof.items() if n}
+    clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": per_step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded N(0,1))", "config": config_dict(world),
+        "timed_blocks": len(block_ms),
+        "ms_per_step_quartiles": step_q,
         "algorithmic_tflops": alg * world / per_step_s / 1e12,
         "effective_tflops": eff * world / per_step_s / 1e12,
         "pct_fp16_peak_algorithmic": 100.0 * alg / per_step_s / 1e12 / peaks["tflops"],
@@ -348,18 +530,35 @@ def main():
                      "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": (achieved / peaks["tflops"]) if achieved else None,
                      "peak_source": f"{peaks['source']} dense bf16 burst (fp16 rate taken equal)",
-                     "launches_per_step": gemm_launches_per_step,
+                     "launches_per_step": gemm_n / args.steps,
                      "avg_launch_ms": gemm_ms / max(1, gemm_n),
-                     "algorithmic_flops_per_launch": alg / max(1e-9, gemm_launches_per_step),
-                     "traffic": traffic},
+                     "algorithmic_flops_per_launch": alg / max(1e-9, gemm_n / args.steps),
+                     "traffic": profiled_traffic()},
         "kernels": kernels,
         "gpu_launches": launches,
-        "clocks": sampler.summary(),
+        "clocks": clocks,
         "e2e": {"value": job_throughput(G * e2e_steps, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": G * R * C * 4,
                 "d2h_bytes_per_step": G * R * C * 4},
     }
+    if clocks.get("sm_mhz"):
+        line["ms_x_sm_mhz"] = per_step_s * 1e3 * clocks["sm_mhz"]
+    if rank == 0 and world == 1 and not args.no_configs:
+        del x
+        torch.cuda.empty_cache()
+        line["configs"] = {
+            "single_128x512": bucket_line(gns, torch, stream, dev, "single_128x512", 1, 128, 512, 200, peaks["tflops"]),
+            "square_16x2048": bucket_line(gns, torch, stream, dev, "square_16x2048 (standard NS)", 16, 2048, 2048, 5,
+                                          peaks["tflops"]),
+            "moe_256x512x2048": bucket_line(gns, torch, stream, dev, "moe_256x512x2048", 256, 512, 2048, 5,
+                                            peaks["tflops"]),
+            "per_head_16x256x4096": bucket_line(gns, torch, stream, dev, "per_head_16x256x4096", 16, 256, 4096, 20,
+                                                peaks["tflops"]),
+            "llama7b_muon_step": llama7b_line(gns, torch, stream, dev, peaks),
+        }
+        line["configs"]["single_128x512"]["us_per_call"] = line["configs"]["single_128x512"]["ms_per_call"] * 1e3
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(bucket, args.cpu_budget)
+        line["cpu_baseline_single_thread"] = single_thread_oracle()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

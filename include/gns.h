@@ -115,8 +115,9 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
  * capture. Every call shares the array, so calls that overlap on the GPU (on
  * different streams) race and must not be issued. Device-side conditions (a
  * non-finite input norm, a bounded wait that ran out) go to a status word
- * inside the array, cleared at the start of each call; gns_get_status() does
- * not read it.
+ * inside the array, which gns_get_status() reads and clears without
+ * allocating. GNS_NUM_SMS caps the SMs used, as for the allocating entry
+ * points.
  */
 int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C, int steps, int restart_at,
                                       const float* coeffs, void* stream);
@@ -224,8 +225,29 @@ int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, i
                   float alpha, float beta, void* stream);
 
 /* Synchronizes `stream`, returns the device status word of the current device
- * as a gns_status (GNS_OK, GNS_ERR_NONFINITE or GNS_ERR_TIMEOUT) and clears it. */
+ * as a gns_status (GNS_OK, GNS_ERR_NONFINITE or GNS_ERR_TIMEOUT) and clears it.
+ * It reads both the allocating entry points' word and, once the
+ * allocation-free entry point has run on the device, that entry point's word
+ * (the first nonzero one is returned, both are cleared); it allocates nothing.
+ * A condition stays recorded until it is read: a non-finite input makes only
+ * its own matrix's output non-finite, and a later call runs normally whether
+ * or not the word has been read. */
 int gns_get_status(void* stream);
+
+/*
+ * gns_test_bounded_wait: a check of the library's failure handling, not part
+ * of the path (the pages have no counterpart; their only failure mode is the
+ * numerical divergence that the restarts prevent). Launches one block of 256
+ * threads on `stream` that wait for something that never happens: an
+ * mbarrier phase no thread completes (kind 0) or a device counter nothing
+ * releases (kind 1). Thread 0 waits at most limit_ns nanoseconds
+ * (1000 .. 1e9); the others wait with a 1000 times longer bound and must give
+ * up through the abort mark thread 0 raises. Synchronizes `stream` and
+ * returns the number of waits that gave up (256 when every wait ended), or a
+ * negative gns_status. Afterwards gns_get_status() reports GNS_ERR_TIMEOUT and
+ * the device stays usable: no fault, no trap, no hang.
+ */
+int gns_test_bounded_wait(int kind, int64_t limit_ns, void* stream);
 
 /* Static text for a gns_status value. */
 const char* gns_status_string(int status);

@@ -37,6 +37,7 @@ PROTOTYPES = {
     "gns_muon_update": (_i, [_vp, _vp, _i, _i, _f, _f, _f, _u64, _u64, _i64, _vp]),
     "gns_symm_gemm": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _f, _vp]),
     "gns_get_status": (_i, [_vp]),
+    "gns_test_bounded_wait": (_i, [_i, _i64, _vp]),
     "gns_status_string": (ctypes.c_char_p, [_i]),
     "gns_last_error": (ctypes.c_char_p, []),
     "gns_workspace_bytes": (_i64, []),

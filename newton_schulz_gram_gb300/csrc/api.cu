@@ -72,7 +72,9 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     char* ws = nullptr;
     size_t ws_bytes = 0;
-    int* err = nullptr;
+    int* err = nullptr;      // status block: [0] status word, [1] abort mark (see DevStatus)
+    int epoch = 0;           // number of the current call on this device
+    DevStatus status{};      // the current call's device-side error reporting
     float* stage = nullptr;  // device staging for the host-buffer entry point
     size_t stage_bytes = 0;
     cudaStream_t h2d = nullptr, d2h = nullptr;  // copy streams of the host-buffer entry point
@@ -104,6 +106,19 @@ int get_state(DeviceState** out) {
     return GNS_OK;
 }
 
+// Bound of every device-side wait: 2 s, or GNS_WAIT_LIMIT_MS.
+unsigned long long wait_limit_ns() {
+    const char* e = std::getenv("GNS_WAIT_LIMIT_MS");
+    if (e && std::atoll(e) > 0) return static_cast<unsigned long long>(std::atoll(e)) * 1000000ull;
+    return kDefaultWaitLimitNs;
+}
+
+// Starts a call on a device: a new epoch for its kernels' abort mark.
+void begin_call(DeviceState& st) {
+    st.epoch = st.epoch == 0x7fffffff ? 1 : st.epoch + 1;
+    st.status = DevStatus{st.err, st.epoch, 0, wait_limit_ns()};
+}
+
 int ensure_workspace(DeviceState& st, size_t bytes) {
     if (st.ws_bytes >= bytes) return GNS_OK;
     if (st.ws) {
@@ -121,6 +136,33 @@ int ensure_workspace(DeviceState& st, size_t bytes) {
     st.ws_bytes = want;
     return GNS_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of gns_orthogonalize_batched.
+//
+// Some callers cannot let the library call cudaMalloc: their device memory is
+// already held by their own allocator or pool, or they cannot accept the
+// device-wide synchronization that growing the cached workspace costs
+// (cudaDeviceSynchronize, cudaFree, cudaMalloc). For them the workspace of
+// this entry point is one fixed array in device memory, declared below, that
+// every GPU which loads the library holds until the process exits.
+
+constexpr size_t kNoAllocBytes = size_t(64) << 20;  // size of the fixed array
+constexpr size_t kNoAllocStatusBytes = 256;         // status word, then the workspace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+    bool ready = false;
+    char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int epoch = 0;            // number of the current allocation-free call on this device
+};
+
+std::mutex g_noalloc_mu;
+std::map<int, NoAllocDevice> g_noalloc;
+
 
 // ------------------------------------------------------- launch accounting
 //
@@ -240,27 +282,22 @@ struct ProblemSpec {
     const MuonFuse* muon = nullptr;  // fused Muon update instead of storing D
 };
 
-// Tile shape for a program: 256 x 256 tiles on CTA pairs (two pairs per
-// cluster for n >= 3072) when the matrices fill them; else 128 x 128 tiles on
-// single CTAs.
-// GNS_TILE=128x1|256x1|256x2|256x2x2 forces one shape (tuning). With two
-// pairs per cluster, non-symmetric products share their A operand between
-// the pairs (multicast); symmetric ones only when GNS_SHARE_SYM=1 (their
-// rows must then be padded to an even tile count).
+// Tile shape for a program: 256 x 256 tiles on CTA pairs when the matrices
+// fill them; else 128 x 128 tiles on single CTAs.
+// GNS_TILE=128x1|256x1|256x2 forces one shape (tuning).
 struct TileShape {
-    int bn, cg, np;
+    int bn, cg;
 };
 
 TileShape choose_tile(int n, int G, int num_sms) {
     const char* force = std::getenv("GNS_TILE");
     if (force) {
         const std::string f(force);
-        if (f == "128x1") return {128, 1, 1};
-        if (f == "256x1") return {256, 1, 1};
-        if (f == "256x2") return {256, 2, 1};
-        if (f == "256x2x2") return {256, 2, 2};
+        if (f == "128x1") return {128, 1};
+        if (f == "256x1") return {256, 1};
+        if (f == "256x2") return {256, 2};
     }
-    if (n < 192) return {128, 1, 1};
+    if (n < 192) return {128, 1};
     // A bucket whose n x n products give the CTA pairs less than about one and
     // a half waves of 256 x 256 tiles leaves pairs idle: single-CTA 128 x 128
     // tiles quadruple the tile count (measured: 16 x 256 x 4096, 32 x 384 x 1536
@@ -268,10 +305,8 @@ TileShape choose_tile(int n, int G, int num_sms) {
     // 256 x 512 x 2048 slower).
     const long long t2 = (n + 255) / 256;
     const long long pair_tiles = static_cast<long long>(G) * t2 * (t2 + 1) / 2;
-    if (2 * pair_tiles < 3LL * (num_sms / 2)) return {128, 1, 1};
-    // Two pairs per cluster (A shared) pay off only for large matrices: the
-    // 4-CTA clusters leave 8 of the 152 SMs idle.
-    return n >= 3072 ? TileShape{256, 2, 2} : TileShape{256, 2, 1};
+    if (2 * pair_tiles < 3LL * (num_sms / 2)) return {128, 1};
+    return {256, 2};
 }
 
 // Non-symmetric products walk their tiles column by column unless
@@ -279,11 +314,6 @@ TileShape choose_tile(int n, int G, int num_sms) {
 bool col_walk() {
     const char* e = std::getenv("GNS_COL_WALK");
     return !(e && std::atoi(e) == 0);
-}
-
-bool share_symmetric() {
-    const char* e = std::getenv("GNS_SHARE_SYM");
-    return e && std::atoi(e) != 0;
 }
 
 // Collects the phases of one launch. Tensor maps are shared between the
@@ -333,10 +363,10 @@ class ProgramBuilder {
         } else {
             prog_.counters = nullptr;
         }
-        prog_.err = st_.err;
+        prog_.st = st_.status;
         prog_.G = G_;
         cudaStream_t s = s_;
-        LAUNCH(kClsGemm, launch_gemm_program(prog_, ts_.bn, ts_.cg, ts_.np, st_.num_sms, s));
+        LAUNCH(kClsGemm, launch_gemm_program(prog_, ts_.bn, ts_.cg, st_.num_sms, s));
         reset();
         return GNS_OK;
     }
@@ -394,9 +424,7 @@ class ProgramBuilder {
         if ((sp.a_sym || sp.b_sym || sp.lower) && bn != 128 * cg)
             return fail(GNS_ERR_INVALID, "lower-only storage needs square tiles");
         if ((sp.a_sym && sp.a_mn) || (sp.b_sym && sp.b_mn)) return fail(GNS_ERR_INVALID, "lower-only operands are K-major");
-        const bool share = ts_.np == 2 && (!sp.sym || share_symmetric());
-        // With two pairs sharing A, each pair loads 64 of a CTA's 128 A rows.
-        RET(operand(sp.A, (sp.a_mn || share) ? 64u : 128u, pr.mA, sp.a_mn));
+        RET(operand(sp.A, sp.a_mn ? 64u : 128u, pr.mA, sp.a_mn));
         RET(operand(sp.B, sp.b_mn ? 64u : static_cast<uint32_t>(bn / cg), pr.mB, sp.b_mn));
         if (sp.muon) {
             if (sp.sym || sp.Dt || sp.D2) return fail(GNS_ERR_INVALID, "the fused update needs a plain product");
@@ -419,8 +447,7 @@ class ProgramBuilder {
         }
         if (sp.lower) flags |= kFlagLower;
         if (sp.muon) flags |= kFlagMuon;
-        if (share) flags |= kFlagShareA;
-        if (!sp.sym && !share && col_walk()) flags |= kFlagColWalk;
+        if (!sp.sym && col_walk()) flags |= kFlagColWalk;
         if (sp.C) {
             flags |= kFlagC;
             pr.C = static_cast<const __half*>(sp.C->p);
@@ -448,7 +475,7 @@ class ProgramBuilder {
         pr.K = Ka;
         pr.tiles_n = (pr.N + bn - 1) / bn;
         pr.tiles_m = (pr.M + 128 * cg - 1) / (128 * cg);
-        pr.tiles_per_matrix = gemm_tiles_per_matrix(pr.M, pr.N, bn, cg, sp.sym, ts_.np, share, &pr.tiles_n_walk);
+        pr.tiles_per_matrix = gemm_tiles_per_matrix(pr.M, pr.N, bn, cg, sp.sym, &pr.tiles_n_walk);
         pr.flags = flags;
         return GNS_OK;
     }
@@ -615,7 +642,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
         job.stride_out = Xa.stride;
         job.partial = reinterpret_cast<float*>(ws + L.partial);
         job.queue = reinterpret_cast<int*>(ws + L.queue);
-        job.err = st.err;
+        job.st = st.status;
         LAUNCH(kClsNorm, launch_norm_cast(job, st.num_sms, s));
     }
     const float inv_s = 1.0f / g.s;
@@ -833,6 +860,7 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, uint64_t re
     if (!ptr) return fail(GNS_ERR_INVALID, "ptr is null");
     DeviceState* st = nullptr;
     RET(get_state(&st));
+    begin_call(*st);
     Coeffs cf;
     RET(load_coeffs(coeffs, steps, cf));
     const BucketGeom g = make_geom(R, C);
@@ -897,6 +925,7 @@ int optimizer_step(const gns_tensor* params, const gns_tensor* grads, const gns_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DeviceState* st = nullptr;
     RET(get_state(&st));
+    begin_call(*st);
     // Buckets of equal (rows, cols), in order of first appearance.
     std::vector<std::pair<std::pair<int, int>, std::vector<int>>> buckets;
     for (int i = 0; i < n; ++i) {
@@ -1017,6 +1046,7 @@ int dion3_step_impl(const gns_tensor* params, const gns_tensor* grads, const gns
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     DeviceState* st = nullptr;
     RET(get_state(&st));
+    begin_call(*st);
     std::vector<std::pair<std::pair<int, int>, std::vector<int>>> buckets;
     for (int i = 0; i < n; ++i) {
         auto key = std::make_pair(params[i].rows, params[i].cols);
@@ -1277,6 +1307,7 @@ int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, i
         if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return fail(GNS_ERR_INVALID, "pointers must be 16-byte aligned");
     DeviceState* st = nullptr;
     RET(get_state(&st));
+    begin_call(*st);
     Mat a{const_cast<void*>(A), n, k, k, static_cast<long long>(n) * k, false};
     Mat b{const_cast<void*>(B), n, k, k, static_cast<long long>(n) * k, false};
     Mat d{D, n, n, n, static_cast<long long>(n) * n, false};
@@ -1297,12 +1328,56 @@ int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, i
 }
 
 int gns_get_status(void* stream) {
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    // The status words of this device: the allocating entry points' and the
+    // allocation-free entry point's (inside its fixed array). Neither is
+    // created here, so this call allocates nothing.
+    int* words[2] = {nullptr, nullptr};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end()) words[0] = it->second.err;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        auto it = g_noalloc.find(dev);
+        if (it != g_noalloc.end() && it->second.ready) words[1] = reinterpret_cast<int*>(it->second.scratch);
+    }
+    int result = GNS_OK;
+    for (int* w : words) {
+        if (!w) continue;
+        int v = 0;
+        CK(cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost));
+        if (v != 0) {
+            CK(cudaMemset(w, 0, sizeof(int)));
+            if (result == GNS_OK) result = v;
+        }
+    }
+    return result;
+}
+
+int gns_test_bounded_wait(int kind, int64_t limit_ns, void* stream) {
+    if (kind < 0 || kind > 1) return fail(GNS_ERR_INVALID, "kind must be 0 (mbarrier) or 1 (counter)");
+    if (limit_ns < 1000 || limit_ns > 1000000000LL) return fail(GNS_ERR_INVALID, "limit_ns must be in [1 us, 1 s]");
     DeviceState* st = nullptr;
     RET(get_state(&st));
-    CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    begin_call(*st);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DevStatus first = st->status;
+    first.limit_ns = static_cast<unsigned long long>(limit_ns);
+    DevStatus rest = first;
+    rest.limit_ns = std::min<unsigned long long>(1000ull * first.limit_ns, 10000000000ull);
+    // Words 2 and 3 of the status block: a counter nothing writes (zero since
+    // the block was allocated) and the count of waits that gave up.
+    const int* never = st->err + 2;
+    int* gave_up = st->err + 3;
+    CK(cudaMemsetAsync(gave_up, 0, sizeof(int), s));
+    LAUNCH(kClsMuon, launch_bounded_wait_test(first, rest, kind, never, gave_up, s));
+    CK(cudaStreamSynchronize(s));
     int v = 0;
-    CK(cudaMemcpy(&v, st->err, sizeof(int), cudaMemcpyDeviceToHost));
-    CK(cudaMemset(st->err, 0, sizeof(int)));
+    CK(cudaMemcpy(&v, gave_up, sizeof(int), cudaMemcpyDeviceToHost));
     return v;
 }
 
@@ -1393,37 +1468,6 @@ void gns_release(void) {
 
 }  // extern "C"
 
-// ---------------------------------------------------------------------------
-// Allocation-free variant of gns_orthogonalize_batched.
-//
-// Some callers cannot let the library call cudaMalloc: their device memory is
-// already held by their own allocator or pool, or they cannot accept the
-// device-wide synchronization that growing the cached workspace costs
-// (cudaDeviceSynchronize, cudaFree, cudaMalloc). For them the workspace of
-// this entry point is one fixed array in device memory, declared below, that
-// every GPU which loads the library holds until the process exits.
-
-namespace gns {
-namespace {
-
-constexpr size_t kNoAllocBytes = size_t(64) << 20;  // size of the fixed array
-constexpr size_t kNoAllocStatusBytes = 256;         // status word, then the workspace
-
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
-
-struct NoAllocDevice {
-    bool ready = false;
-    char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-    int num_sms = 0;
-    int cc_major = 0, cc_minor = 0;
-};
-
-std::mutex g_noalloc_mu;
-std::map<int, NoAllocDevice> g_noalloc;
-
-}  // namespace
-}  // namespace gns
-
 extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C, int steps, int restart_at,
                                                  const float* coeffs, void* stream) {
     RET(validate_common(G, R, C, steps));
@@ -1440,6 +1484,9 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
         NoAllocDevice& e = g_noalloc[dev];
         if (!e.ready) {
             CK(cudaDeviceGetAttribute(&e.num_sms, cudaDevAttrMultiProcessorCount, dev));
+            // The same SM cap as the allocating entry points (GNS_NUM_SMS).
+            const char* cap = std::getenv("GNS_NUM_SMS");
+            if (cap && std::atoi(cap) > 0) e.num_sms = std::min(e.num_sms, std::atoi(cap));
             CK(cudaDeviceGetAttribute(&e.cc_major, cudaDevAttrComputeCapabilityMajor, dev));
             CK(cudaDeviceGetAttribute(&e.cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
             void* addr = nullptr;
@@ -1447,6 +1494,7 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
             e.scratch = static_cast<char*>(addr);
             e.ready = true;
         }
+        e.epoch = e.epoch == 0x7fffffff ? 1 : e.epoch + 1;
         nd = e;
     }
     if (!(nd.cc_major == 10 && nd.cc_minor == 3))
@@ -1472,11 +1520,16 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
     st.cc_major = nd.cc_major;
     st.cc_minor = nd.cc_minor;
     st.err = reinterpret_cast<int*>(nd.scratch);
+    st.epoch = nd.epoch;
+    st.status = DevStatus{st.err, st.epoch, 0, wait_limit_ns()};
     st.ws = nd.scratch + kNoAllocStatusBytes;
     st.ws_bytes = avail;
-    // The array keeps the previous call's contents; only the status word must
-    // start at zero (every workspace byte a kernel reads is written first).
-    CK(cudaMemsetAsync(st.err, 0, sizeof(int), s));
+    // The array keeps the previous call's contents. The status word starts at
+    // zero (the array is zero when the library loads) and is cleared by
+    // gns_get_status; the abort mark holds an earlier call's number, which no
+    // later call's waits take for their own; every workspace byte a kernel
+    // reads is written first in the same call (the counters and queues by
+    // the stream-ordered clears inside the call).
 
     const long long numel = static_cast<long long>(R) * C;
     for (int g0 = 0; g0 < G; g0 += Gc) {

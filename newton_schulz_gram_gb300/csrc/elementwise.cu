@@ -27,6 +27,7 @@ namespace gns {
 namespace {
 
 constexpr int kThreads = 256;
+static_assert(kBoundedWaitThreads == kThreads, "the bounded-wait check runs one block of kThreads");
 
 // Launch with the programmatic-dependent-launch attribute; every kernel here
 // starts with grid_dependency_wait(), so it reads nothing the previous grid
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_con
                 // Every part of matrix g summed: fixed-order sum of its partials
                 // (the same in every cast item of g).
                 bool ok = true;
-                if (lane == 0) ok = wait_counter(ready + it.g, a.nparts, a.j.err);
+                if (lane == 0) ok = wait_counter(ready + it.g, a.nparts, a.j.st);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (ok) (void)ld_acquire(ready + it.g);
                 // Lane l adds partials l, l + 32, l + 64, ... in that order; the
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_con
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
                 if (lane == 0) {
                     const float norm = sqrtf(v);
-                    if (ok && !isfinite(norm)) raise_error(a.j.err, kDevErrNonFinite);
+                    if (ok && !isfinite(norm)) raise_error(a.j.st, kDevErrNonFinite);
                     s_scale = ok ? ldexpf(1.0f, a.j.k_exp) / (1.05f * (norm + 1e-7f)) : 0.0f;
                 }
             }
@@ -593,6 +594,26 @@ __global__ void __launch_bounds__(kThreads) normuon_factor_kernel(const float* r
     for (int r = threadIdx.x; r < R; r += kThreads) row_step[off + r] = __fmul_rn(f, inv[off + r]);
 }
 
+// Check of the bounded waits (no part of the path): every thread of one
+// block waits for something that never happens, an mbarrier phase that no
+// thread completes (kind 0) or a counter that nothing releases (kind 1).
+// Thread 0 waits with the bound of `first`; the other threads wait with the
+// much longer bound of `rest` and must give up through the abort mark that
+// thread 0 raises when its own bound runs out. gave_up counts the waits that
+// returned false.
+__global__ void __launch_bounds__(kThreads) bounded_wait_test_kernel(DevStatus first, DevStatus rest, int kind,
+                                                                     const int* never, int* gave_up) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const DevStatus st = threadIdx.x == 0 ? first : rest;
+    const bool ok = kind == 0 ? mbar_wait(smem_u32(&bar), 0, st) : wait_counter(never, 1, st);
+    if (!ok) atomicAdd(gave_up, 1);
+}
+
 int grid_for(long long work, int per_block_items) {
     long long b = (work + per_block_items - 1) / per_block_items;
     if (b < 1) b = 1;
@@ -675,6 +696,11 @@ int launch_normuon_factor(const float* row_sq, const float* row_hat, const float
     if (count <= 0 || R <= 0) return cudaSuccess;
     return launch_pdl(normuon_factor_kernel, dim3(count), dim3(kThreads), s, row_sq, row_hat, inv, R, lr_scale,
                       row_step);
+}
+
+int launch_bounded_wait_test(const DevStatus& first, const DevStatus& rest, int kind, const int* never,
+                             int* gave_up, cudaStream_t s) {
+    return launch_pdl(bounded_wait_test_kernel, dim3(1), dim3(kThreads), s, first, rest, kind, never, gave_up);
 }
 
 int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o, const long long* base_dev,

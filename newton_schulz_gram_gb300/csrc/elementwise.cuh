@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ptx.cuh"
+
 namespace gns {
 
 // A set of G matrices: either contiguous (base + g * stride) or a device
@@ -49,7 +51,7 @@ struct NormCastJob {
     long long ld_out, stride_out;
     float* partial;
     int* queue;
-    int* err;
+    DevStatus st;
 };
 
 int launch_norm_cast(const NormCastJob& job, int num_sms, cudaStream_t s);
@@ -82,5 +84,13 @@ int launch_normuon_rows(const MatrixSet& O, long long ld_o, const MatrixSet& V, 
                         float eps, float* row_sq, float* row_hat, float* inv, cudaStream_t s);
 int launch_normuon_factor(const float* row_sq, const float* row_hat, const float* inv, int count, int R,
                           float lr_scale, float* row_step, cudaStream_t s);
+
+// The bounded-wait check: one block of kBoundedWaitThreads threads waits on
+// an mbarrier phase (kind 0) or a counter `never` (kind 1, stays zero) that
+// nothing completes; thread 0 with `first`'s bound, the others with `rest`'s.
+// Adds one to *gave_up for every wait that gave up.
+constexpr int kBoundedWaitThreads = 256;
+int launch_bounded_wait_test(const DevStatus& first, const DevStatus& rest, int kind, const int* never,
+                             int* gave_up, cudaStream_t s);
 
 }  // namespace gns

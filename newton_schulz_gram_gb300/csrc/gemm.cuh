@@ -19,6 +19,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include "ptx.cuh"
+
 namespace gns {
 
 enum GemmFlags : int {
@@ -29,8 +31,6 @@ enum GemmFlags : int {
     kFlagOutF32 = 16, // D is fp32 (otherwise fp16)
     kFlagAmn = 32,    // A is MN-major: the stored matrix is K x M (A^T row-major)
     kFlagBmn = 64,    // B is MN-major: the stored matrix is K x N (B^T row-major)
-    kFlagShareA = 128, // two CTA pairs of a cluster compute horizontally adjacent tiles
-                       // and share (multicast) their A operand
     // Symmetric matrices stored lower-only: only tiles (I, J) with J <= I of
     // a square tiling (edge = the tile's M edge, which then equals BN) hold
     // data, diagonal tiles in full. An operand flagged so reads a k-block in
@@ -79,9 +79,9 @@ struct GemmProblem {
     float alpha, beta, delta, gamma;
     int M, N, K;
     int tiles_n;           // tile columns of the matrix
-    int tiles_n_walk;      // tile columns enumerated per row (tiles_n, or even with kFlagShareA)
+    int tiles_n_walk;      // tile columns enumerated per row (= tiles_n)
     int tiles_m;           // tile rows of the matrix
-    int tiles_per_matrix;  // tiles enumerated per matrix (even when pairs share a cluster)
+    int tiles_per_matrix;  // tiles enumerated per matrix
     int flags;
     // Indices into GemmProgram::maps (-1 when unused). K-major operand maps:
     // box {64 (K), rows per CTA}; MN-major operand maps: box {64 (M or N),
@@ -105,23 +105,21 @@ struct alignas(128) GemmProgram {
     GemmProblem prob[kMaxProblems];
     GemmPhaseDesc phase[kMaxPhases];
     int* counters;  // [G] completed-tile counters, zero at launch; null for one phase
-    int* err;
+    DevStatus st;
     int nmaps, nprob, nphase, G, total_tiles;
 };
 
 // Host-side launcher (gemm_tc.cu). Tile shapes: cg = 1 and bn = 128 or 256
 // (one CTA, 128 x bn tiles), or cg = 2 and bn = 256 (a CTA pair, 256 x 256
-// tiles with paired MMAs); np = 2 (with cg = 2) groups two pairs per cluster,
-// which then compute consecutive tiles in lock-step and may share A. Launches
-// carry the programmatic-dependent-launch attribute; the kernel waits for the
-// previous grid before reading its operands. Returns a cudaError_t value.
-int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int np, int num_sms, cudaStream_t stream);
+// tiles with paired MMAs). Launches carry the programmatic-dependent-launch
+// attribute; the kernel waits for the previous grid before reading its
+// operands. Returns a cudaError_t value.
+int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream);
 int gemm_smem_bytes(int bn, int cg);
-// Tile walk of one matrix of an M x N problem: lower-triangle tiles if sym;
-// rows padded to an even tile count when share; the total padded to even
-// when np = 2. Returns tiles per matrix and sets *walk_n (tiles per row walked
-// for non-symmetric problems).
-int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym, int np, bool share, int* walk_n);
+// Tile walk of one matrix of an M x N problem: lower-triangle tiles if sym.
+// Returns tiles per matrix and sets *walk_n (tiles per row walked for
+// non-symmetric problems).
+int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym, int* walk_n);
 // Counter increments one tile contributes (one per epilogue warp).
 int gemm_signals_per_tile(int cg);
 

@@ -98,12 +98,10 @@ struct TileInfo {
     int p, g, m0, n0, s;  // problem, matrix, tile origin, phase
 };
 
-// Column blocks a symmetric row block of height tm touches: j * bn <= tm i + tm - 1
-// (rounded up to even when two CTA pairs share the row's A).
-__host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int tiles_n, bool share) {
-    int c = (tm * i + tm - 1) / bn + 1;
-    c = c < tiles_n ? c : tiles_n;
-    return share ? c + (c & 1) : c;
+// Column blocks a symmetric row block of height tm touches: j * bn <= tm i + tm - 1.
+__host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int tiles_n) {
+    const int c = (tm * i + tm - 1) / bn + 1;
+    return c < tiles_n ? c : tiles_n;
 }
 
 // Decodes program tiles for one role. A role visits the tiles first,
@@ -166,18 +164,17 @@ struct TileWalker {
         int i, j;
         // Tiles past the real ones (padding) decode to out-of-range tiles: their
         // loads read zeros and their epilogue writes nothing.
-        if ((flags & kFlagSym) && TM == BN && !(flags & kFlagShareA)) {
+        if ((flags & kFlagSym) && TM == BN) {
             // Square tiles: row block i holds i + 1 tiles, i (i + 1) / 2 before it.
             i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
             if (i * (i + 1) / 2 > t) --i;
             if ((i + 1) * (i + 2) / 2 <= t) ++i;
             j = t - i * (i + 1) / 2;
         } else if (flags & kFlagSym) {
-            const bool share = flags & kFlagShareA;
             int acc = 0;
             i = 0;
             while (true) {
-                const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n, share);
+                const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n);
                 if (t < acc + cnt) break;
                 acc += cnt;
                 ++i;
@@ -219,18 +216,17 @@ __device__ __forceinline__ TileInfo decode_tile(const CtlPhase* cph, const CtlPr
     }
     const int flags = cpb[p].flags;
     int i, j;
-    if ((flags & kFlagSym) && TM == BN && !(flags & kFlagShareA)) {
+    if ((flags & kFlagSym) && TM == BN) {
         i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
         while (i * (i + 1) / 2 > t) --i;
         while ((i + 1) * (i + 2) / 2 <= t) ++i;
         j = t - i * (i + 1) / 2;
     } else if (flags & kFlagSym) {
-        const bool share = flags & kFlagShareA;
         const int tiles_n = cpb[p].tiles_n;
         int acc = 0;
         i = 0;
         while (true) {
-            const int cnt = sym_row_tiles(i, TM, BN, tiles_n, share);
+            const int cnt = sym_row_tiles(i, TM, BN, tiles_n);
             if (t < acc + cnt) break;
             acc += cnt;
             ++i;
@@ -472,18 +468,17 @@ __device__ __forceinline__ void muon_update_row(const GemmProblem& pr, int g, in
     }
 }
 
-// Waits for an mbarrier phase during teardown, ignoring the error word.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+// Waits for an mbarrier phase during teardown, ignoring the abort mark.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kWaitLimitNs) break;
+        if (globaltimer() - t0 > limit_ns) break;
     }
 }
 
-template <int BN, int CG, int NP>
+template <int BN, int CG>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmProgram P) {
-    static_assert(NP == 1 || CG == 2, "pairs per cluster needs paired MMAs");
-    constexpr int CL = CG * NP;  // CTAs per cluster
+    constexpr int CL = CG;  // CTAs per cluster: one pair, or one CTA
     constexpr int STAGES = Cfg<BN, CG>::STAGES;
     constexpr int NCH = BN / 32;
     constexpr int BNH = BN / CG;  // rows of B this CTA stages
@@ -513,23 +508,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    int* err = P.err;
+    const DevStatus& err = P.st;
     const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0;  // rank in the cluster
     const uint32_t rank = crank & (CG - 1);                  // rank in the pair: 0 = leader
     const uint32_t lead = crank & ~uint32_t(CG - 1);         // cluster rank of the pair leader
-    const int pair = static_cast<int>(crank >> 1) & (NP - 1);  // pair within the cluster
     const int unit = blockIdx.x / CL;                        // this cluster's tile walker
     const int units = gridDim.x / CL;
-    const int nwalk = P.total_tiles / NP;                    // super-tiles: NP consecutive tiles
+    const int nwalk = P.total_tiles;
     const int nphase = P.nphase;
     const int G = P.G;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            // With two pairs per cluster every stage is released by both
-            // pairs' MMAs (a shared A half lands in both pairs).
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, NP);
+            mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -575,9 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units * NP);
+            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units);
             for (int w = unit; w < nwalk && ok; w += units) {
-                const TileInfo t = walk.decode(w * NP + pair);
+                const TileInfo t = walk.decode(w);
                 const CtlProb& pr = walk.prob();
                 const CUtensorMap* mapA = &P.maps[pr.mA];
                 const CUtensorMap* mapB = &P.maps[pr.mB];
@@ -588,7 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const CUtensorMap* mapAt = a_sym ? &P.maps[pr.mAt] : mapA;
                 const CUtensorMap* mapBt = b_sym ? &P.maps[pr.mBt] : mapB;
                 const int ti = t.m0 / TM, tj = t.n0 / TM;
-                const bool share = (NP == 2) && (pr.flags & kFlagShareA);
                 const int kblocks = (pr.K + BK - 1) / BK;
                 if (P.counters && t.s > 0) {
                     // The operands of this phase are outputs of earlier phases on
@@ -621,18 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         // All halves complete on the pair leader's barrier.
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (A_BYTES + B_BYTES));
                         const uint32_t lead_fb = map_to_rank(fb, lead);
-                        if (!share) {
-                            load_operand(1, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g);
-                        } else {
-                            // The two pairs need the same 128 A rows in their
-                            // same-rank CTAs: each pair loads one 64-row half
-                            // (one 64 x 64 box, 8 KB) and multicasts it to both,
-                            // so every CTA issues the same number of bytes.
-                            const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2 + rank)));
-                            const int r = arow + 64 * pair;
-                            tma_load_3d_multicast_pair(smem_u32(sA + stage * A_BYTES) + pair * kMnBlockBytes, mA_k,
-                                                       lead_fb, a_mn ? r : kb * BK, a_mn ? kb * BK : r, t.g, mask);
-                        }
+                        load_operand(1, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g);
                         load_operand(1, smem_u32(sB + stage * B_BYTES), mB_k, lead_fb, b_mn, brow, BNH, kb, t.g);
                     }
                     ++issued;
@@ -652,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         phase ^= 1;
                     }
                     --stage;
-                    drain_wait(full0 + 8 * stage, phase);
+                    drain_wait(full0 + 8 * stage, phase, err.limit_ns);
                 }
             }
         }
@@ -663,15 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int iter = 0;
             bool ok = true;
-            constexpr uint16_t kStageMask = (NP == 2) ? 0xF : 0x3;  // both pairs' CTAs
-            const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
-            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units * NP);
+            constexpr uint16_t kPairMask = 0x3;  // both CTAs of the pair
+            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units);
             // Stage-0 descriptors of both operand layouts; a stage adds its
             // byte offset / 16 to the start-address field (addresses < 256 KB).
             const uint64_t ak0 = sw128_kmajor_desc(smem_u32(sA)), amn0 = sw128_mnmajor_desc(smem_u32(sA), kMnBlockBytes);
             const uint64_t bk0 = sw128_kmajor_desc(smem_u32(sB)), bmn0 = sw128_mnmajor_desc(smem_u32(sB), kMnBlockBytes);
             for (int w = unit; w < nwalk && ok; w += units, ++iter) {
-                const TileInfo t = walk.decode(w * NP + pair);
+                const TileInfo t = walk.decode(w);
                 const int pflags = walk.prob().flags;
                 const int kblocks = (walk.prob().K + BK - 1) / BK;
                 const int buf = iter & 1;
@@ -706,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     if constexpr (CG == 1)
                         tc_commit<1>(empty0 + 8 * stage);
                     else
-                        tc_commit_pair(empty0 + 8 * stage, kStageMask);
+                        tc_commit_pair(empty0 + 8 * stage, kPairMask);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -716,11 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 if constexpr (CG == 1)
                     tc_commit<1>(accf0 + 8 * buf);
                 else
-                    tc_commit_pair(accf0 + 8 * buf, pair_mask);
+                    tc_commit_pair(accf0 + 8 * buf, kPairMask);
             }
             // All MMAs issued by this thread must finish before TMEM is freed.
             tc_commit<CG>(drain_bar);
-            drain_wait(drain_bar, 0);
+            drain_wait(drain_bar, 0, err.limit_ns);
         }
         __syncwarp();
     } else {
@@ -739,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         bool ok = true;
         int ps = 0;
         for (int w = unit; w < nwalk && ok; w += units, ++iter) {
-            const TileInfo t = decode_tile<BN, CG>(cph, cpb, nphase, G, w * NP + pair, ps);
+            const TileInfo t = decode_tile<BN, CG>(cph, cpb, nphase, G, w, ps);
             const GemmProblem& pr = P.prob[t.p];
             const int buf = iter & 1;
             const int flags = cpb[t.p].flags;
@@ -892,16 +871,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         // C loads still in flight (only after a failed wait) land before exit.
         if (lane == 0) {
             for (int kk = 0; kk < 2; ++kk)
-                if (cpend & (1u << kk)) drain_wait(cbw + 8 * kk, (cpar >> kk) & 1);
+                if (cpend & (1u << kk)) drain_wait(cbw + 8 * kk, (cpar >> kk) & 1, err.limit_ns);
         }
         __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
-    // The leader's MMAs read the peer's shared memory, multicasts write into
-    // other CTAs and epilogues arrive on the leader's barriers: no CTA of the
-    // cluster leaves before all are done.
+    // The leader's MMAs read the peer's shared memory and the peer's loads
+    // and epilogues arrive on the leader's barriers: no CTA of the cluster
+    // leaves before all are done.
     if constexpr (CL > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
@@ -909,51 +888,66 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
 }
 
-// Clusters of CL CTAs that can be resident at once with this kernel's
-// shared memory; the grid never exceeds it, so every cluster of a program
-// runs concurrently (tiles wait on tiles of other clusters).
-template <int BN, int CG, int NP>
-int max_clusters(int num_sms) {
-    static int cached = -1;
-    if (cached < 0) {
-        constexpr int CL = CG * NP;
+// Per-device launch state of one kernel variant: the dynamic shared-memory
+// opt-in is a per-device function attribute, and the resident cluster count
+// is a property of the device, so both are kept per device ordinal.
+constexpr int kMaxDevices = 64;
+
+struct VariantState {
+    bool configured = false;
+    int clusters = -1;
+};
+
+template <int BN, int CG>
+VariantState& variant_state(int dev) {
+    static VariantState st[kMaxDevices];
+    return st[dev];
+}
+
+// Clusters of CG CTAs that can be resident at once with this kernel's
+// shared memory on the current device; the grid never exceeds it, so every
+// cluster of a program runs concurrently (tiles wait on tiles of other
+// clusters).
+template <int BN, int CG>
+int max_clusters(VariantState& vs, int num_sms) {
+    if (vs.clusters < 0) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(CL * (num_sms / CL));
+        cfg.gridDim = dim3(CG * (num_sms / CG));
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem_bytes<BN, CG>();
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.x = CG;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, CG, NP>, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, CG>, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
-            n = num_sms / CL;
+            n = num_sms / CG;
         }
-        cached = n;
+        vs.clusters = n;
     }
-    return cached < num_sms / (CG * NP) ? cached : num_sms / (CG * NP);
+    return vs.clusters < num_sms / CG ? vs.clusters : num_sms / CG;
 }
 
-template <int BN, int CG, int NP>
+template <int BN, int CG>
 int launch_impl(const GemmProgram& prog, int num_sms, cudaStream_t stream) {
-    static bool configured = false;
     constexpr int bytes = smem_bytes<BN, CG>();
-    constexpr int CL = CG * NP;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(gemm_tc_kernel<BN, CG, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    VariantState& vs = variant_state<BN, CG>(dev);
+    if (!vs.configured) {
+        e = cudaFuncSetAttribute(gemm_tc_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
-        configured = true;
+        vs.configured = true;
     }
     if (prog.total_tiles <= 0) return cudaSuccess;
-    if (prog.total_tiles % NP != 0) return cudaErrorInvalidValue;
-    const int walks = prog.total_tiles / NP;
-    const int clusters = max_clusters<BN, CG, NP>(num_sms);
-    const int grid = CL * (walks < clusters ? walks : clusters);
+    const int clusters = max_clusters<BN, CG>(vs, num_sms);
+    const int grid = CG * (prog.total_tiles < clusters ? prog.total_tiles : clusters);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -963,12 +957,12 @@ int launch_impl(const GemmProgram& prog, int num_sms, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.x = CG;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, CG, NP>, prog);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, CG>, prog);
 }
 
 }  // namespace
@@ -978,31 +972,26 @@ int gemm_smem_bytes(int bn, int cg) {
     return bn == 256 ? smem_bytes<256, 1>() : smem_bytes<128, 1>();
 }
 
-int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym, int np, bool share, int* walk_n) {
+int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym, int* walk_n) {
     const int tmh = BM * cg;
     const int tm = (M + tmh - 1) / tmh;
     const int tn = (N + bn - 1) / bn;
-    const int wn = share ? tn + (tn & 1) : tn;
-    if (walk_n) *walk_n = wn;
+    if (walk_n) *walk_n = tn;
     int total = 0;
     if (!sym) {
-        total = tm * wn;
+        total = tm * tn;
     } else {
-        for (int i = 0; i < tm; ++i) total += sym_row_tiles(i, tmh, bn, tn, share);
+        for (int i = 0; i < tm; ++i) total += sym_row_tiles(i, tmh, bn, tn);
     }
-    if (np == 2) total += total & 1;
     return total;
 }
 
 int gemm_signals_per_tile(int cg) { return kEpiWarps * cg; }
 
-int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int np, int num_sms, cudaStream_t stream) {
-    if (cg == 2) {
-        if (np == 2) return launch_impl<256, 2, 2>(prog, num_sms, stream);
-        return launch_impl<256, 2, 1>(prog, num_sms, stream);
-    }
-    if (bn == 256) return launch_impl<256, 1, 1>(prog, num_sms, stream);
-    return launch_impl<128, 1, 1>(prog, num_sms, stream);
+int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream) {
+    if (cg == 2) return launch_impl<256, 2>(prog, num_sms, stream);
+    if (bn == 256) return launch_impl<256, 1>(prog, num_sms, stream);
+    return launch_impl<128, 1>(prog, num_sms, stream);
 }
 
 }  // namespace gns

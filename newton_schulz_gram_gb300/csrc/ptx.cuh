@@ -1,10 +1,11 @@
 // Inline-PTX primitives for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
 // tcgen05 (TMEM allocation, MMA, commit, loads) and their descriptors.
 //
-// Every wait here is bounded: after kWaitLimitNs of %globaltimer time (or as
-// soon as another thread has raised the device error word) it gives up,
-// records GNS_ERR_TIMEOUT in the error word and returns false, so a kernel
-// never spins forever.
+// Every wait here is bounded: after DevStatus::limit_ns of %globaltimer time
+// it gives up, records GNS_ERR_TIMEOUT in the status word, raises the abort
+// mark of its call and returns false, so a kernel never spins forever. A
+// wait also gives up as soon as another thread has raised the abort mark of
+// the same call.
 #pragma once
 
 #include <cstdint>
@@ -13,9 +14,23 @@
 
 namespace gns {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kDevErrTimeout = -4;                 // == GNS_ERR_TIMEOUT
-constexpr int kDevErrNonFinite = -3;               // == GNS_ERR_NONFINITE
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kDevErrTimeout = -4;                        // == GNS_ERR_TIMEOUT
+constexpr int kDevErrNonFinite = -3;                      // == GNS_ERR_NONFINITE
+
+// Device-side error reporting of one library call, passed to its kernels by
+// value. word[0] is the status word: the first condition any kernel found
+// (GNS_ERR_NONFINITE or GNS_ERR_TIMEOUT), kept until the host reads and
+// clears it. word[1] is the abort mark: the number (epoch) of the call whose
+// wait ran out. Waits give up early only when word[1] equals their own
+// call's epoch, so neither a non-finite input nor an abort left over from an
+// earlier call stops the waits of a later one.
+struct DevStatus {
+    int* word;
+    int epoch;  // nonzero, different for consecutive calls on a device
+    int pad;
+    unsigned long long limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -27,12 +42,20 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
-__device__ __forceinline__ void raise_error(int* err, int code) {
-    if (err) atomicCAS(err, 0, code);
+__device__ __forceinline__ void raise_error(const DevStatus& st, int code) {
+    if (st.word) atomicCAS(st.word, 0, code);
 }
 
-__device__ __forceinline__ int peek_error(const int* err) {
-    return err ? *reinterpret_cast<const volatile int*>(err) : 0;
+// A wait of this call ran out: record it and make the call's other waits give up.
+__device__ __forceinline__ void raise_timeout(const DevStatus& st) {
+    if (st.word) {
+        atomicCAS(st.word, 0, kDevErrTimeout);
+        atomicExch(st.word + 1, st.epoch);
+    }
+}
+
+__device__ __forceinline__ bool call_aborted(const DevStatus& st) {
+    return st.word && *reinterpret_cast<const volatile int*>(st.word + 1) == st.epoch;
 }
 
 // ----------------------------------------------------------------- mbarrier
@@ -67,14 +90,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // The bounded spin of mbar_wait, out of line.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int* err) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const DevStatus& st) {
     const uint64_t t0 = globaltimer();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (peek_error(err) != 0) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            raise_error(err, kDevErrTimeout);
+        if (call_aborted(st)) return false;
+        if (globaltimer() - t0 > st.limit_ns) {
+            raise_timeout(st);
             return false;
         }
     }
@@ -83,8 +106,8 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 // Waits for the phase with the given parity to complete. Bounded. The first
 // test is inline: on the issue paths the phase is usually complete already,
 // and a call per k-block costs the single issuing thread measurable time.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
-    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, err);
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const DevStatus& st) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, st);
 }
 
 // -------------------------------------------------------------------- TMA
@@ -161,29 +184,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// TMA load written to the same shared-memory offset of every CTA in `mask`
-// (cluster ranks), each completing on its own mbarrier at the same offset.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
-                                                      int c2, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-        : "memory");
-}
-
-// Multicast TMA load for paired MMAs: written to the same offset of every CTA
-// in `mask`; completion is signalled on the mbarrier at offset `bar` of the
-// pair leader of each destination (bar is given as the leader's address).
-__device__ __forceinline__ void tma_load_3d_multicast_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                                           int c1, int c2, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
         : "memory");
 }
 
@@ -352,7 +352,7 @@ __device__ __forceinline__ uint32_t atom_add_acqrel_cta(uint32_t smem_addr, uint
 }
 
 // Spins until *addr >= target (acquire). Bounded like the mbarrier waits.
-static __device__ __noinline__ bool wait_counter(const int* addr, int target, int* err) {
+static __device__ __noinline__ bool wait_counter(const int* addr, int target, const DevStatus& st) {
     if (ld_acquire(addr) >= target) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
@@ -360,9 +360,9 @@ static __device__ __noinline__ bool wait_counter(const int* addr, int target, in
             if (ld_acquire(addr) >= target) return true;
             __nanosleep(64);
         }
-        if (peek_error(err) != 0) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            raise_error(err, kDevErrTimeout);
+        if (call_aborted(st)) return false;
+        if (globaltimer() - t0 > st.limit_ns) {
+            raise_timeout(st);
             return false;
         }
     }

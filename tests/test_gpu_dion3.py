@@ -5,8 +5,10 @@ bar, grouped == single, and the f = 1 case against muon_step."""
 import numpy as np
 import pytest
 
+from gpu_helpers import sr_update_error
 from inputs import generators as gen
 from oracle import dion3 as D3
+from oracle import gram_ns as O
 from oracle import muon as MU
 
 torch = pytest.importorskip("torch")
@@ -61,12 +63,15 @@ def test_dion3_matches_oracle(gns, fraction):
         # The momentum (accumulation, then damping of exactly the selected
         # rows or columns) bit for bit: the GPU selected the same set.
         assert np.array_equal(m_gpu[i], new_m), (i, "momentum / selection")
-        w_old = MU.bf16_bits_to_f32(w_bits).astype(np.float64)
-        got = MU.bf16_bits_to_f32(w_gpu[i]).astype(np.float64) - w_old
-        want = MU.bf16_bits_to_f32(new_w).astype(np.float64) - w_old
-        noise = np.linalg.norm(np.maximum(np.abs(w_old), np.abs(w_old + want)) * 2.0 ** -7) * 2
-        rel = np.linalg.norm(got - want) / np.linalg.norm(want)
-        assert rel <= 3e-2 + noise / np.linalg.norm(want), (i, rel)
+        # The update direction: O on the selected rows (or columns), zero
+        # elsewhere; within the parity bar once the rounding noise is out.
+        cols = r > c
+        full = np.zeros((c, r) if cols else (r, c))
+        full[S] = O
+        if cols:
+            full = full.T
+        ok, est, det = sr_update_error(w_gpu[i], w_bits, full, 0.02, 0.01, MU.update_scale(r, c))
+        assert ok, (i, est, det)
 
 
 def test_dion3_grouped_equals_single_bitwise(gns):
@@ -92,12 +97,14 @@ def test_dion3_full_fraction_matches_muon(gns):
     gns.muon_step(W, [g.cuda() for _, g, _ in inputs], [m.cuda() for _, _, m in inputs], lr=0.02, wd=0.01, mu=0.9,
                   seed=3, step=7, base_indices=bases)
     torch.cuda.synchronize()
-    for i in range(len(shapes)):
-        w_old = MU.bf16_bits_to_f32(bf16_bits(inputs[i][0])).astype(np.float64)
-        a = MU.bf16_bits_to_f32(w_d3[i]).astype(np.float64) - w_old
-        b = MU.bf16_bits_to_f32(bf16_bits(W[i])).astype(np.float64) - w_old
-        noise = np.linalg.norm(np.abs(w_old) * 2.0 ** -7) * 2
-        assert np.linalg.norm(a - b) <= 3e-2 * np.linalg.norm(b) + noise, i
+    for i, (r, c) in enumerate(shapes):
+        # Both against the orthogonalized gradient: O of the permuted rows is
+        # the permuted O, so the f = 1 selection changes rounding only.
+        w_bits = bf16_bits(inputs[i][0])
+        o_ref = O.orthogonalize(MU.bf16_bits_to_f32(bf16_bits(inputs[i][1])).astype(np.float64))
+        for name, got in (("dion3", w_d3[i]), ("muon", bf16_bits(W[i]))):
+            ok, est, det = sr_update_error(got, w_bits, o_ref, 0.02, 0.01, MU.update_scale(r, c))
+            assert ok, (i, name, est, det)
 
 
 def test_dion3_rejects_bad_fraction(gns):

@@ -169,25 +169,22 @@ def test_restart_schedule_entry_point(gns):
 
 
 # Every tile configuration of the GEMM program, forced through GNS_TILE (the
-# library picks one by n otherwise): single-CTA 128 x 128 and 128 x 256 tiles,
-# CTA pairs, and two pairs per cluster sharing A by balanced multicast, also
-# for the symmetric products (GNS_SHARE_SYM=1, rows padded to even tile
-# counts). Ragged rectangular and square buckets, so the clipped stores, the
-# fp32 output with an addend (last standard-NS step) and the lower-only reads
-# all run in each configuration.
-TILE_CONFIGS = [("128x1", "0"), ("256x1", "0"), ("256x2", "0"), ("256x2x2", "0"), ("256x2x2", "1")]
+# library picks one by n otherwise): single-CTA 128 x 128 and 128 x 256 tiles
+# and CTA pairs. Ragged rectangular and square buckets, so the clipped stores,
+# the fp32 output with an addend (last standard-NS step) and the lower-only
+# reads all run in each configuration.
+TILE_CONFIGS = ["128x1", "256x1", "256x2"]
 
 
-@pytest.mark.parametrize("tile,share_sym", TILE_CONFIGS)
+@pytest.mark.parametrize("tile", TILE_CONFIGS)
 @pytest.mark.parametrize("G,R,C", [(2, 520, 1100), (2, 1100, 520), (2, 384, 384)])
-def test_forced_tile_configs_match_oracle(gns, monkeypatch, tile, share_sym, G, R, C):
+def test_forced_tile_configs_match_oracle(gns, monkeypatch, tile, G, R, C):
     monkeypatch.setenv("GNS_TILE", tile)
-    monkeypatch.setenv("GNS_SHARE_SYM", share_sym)
     X = gen.gaussian_bucket(G, R, C, seed=700 + R + C)
     out = run_gpu(gns, X)
     for g in range(G):
         ref = O.orthogonalize(X[g].astype(np.float64))
-        assert_parity(out[g], ref, what=f"{tile}/{share_sym} {R}x{C}[{g}]")
+        assert_parity(out[g], ref, what=f"{tile} {R}x{C}[{g}]")
 
 
 def test_result_independent_of_tile_config(gns, monkeypatch):
@@ -199,17 +196,15 @@ def test_result_independent_of_tile_config(gns, monkeypatch):
     for G, R, C in ((3, 520, 1100), (2, 1024, 2048), (2, 384, 384)):
         X = gen.gaussian_bucket(G, R, C, seed=900 + R)
         outs = {}
-        for tile, share in TILE_CONFIGS:
+        for tile in TILE_CONFIGS:
             monkeypatch.setenv("GNS_TILE", tile)
-            monkeypatch.setenv("GNS_SHARE_SYM", share)
-            outs[(tile, share)] = run_gpu(gns, X)
-        ref = outs[("256x2", "0")]
+            outs[tile] = run_gpu(gns, X)
+        ref = outs["256x2"]
         for key, out in outs.items():
             assert np.array_equal(out, ref), (G, R, C, key)
     # Grouped (CTA-pair tiles) against single (128 x 128 tiles, chosen for a
     # lone matrix) with the library's own choice.
     monkeypatch.delenv("GNS_TILE", raising=False)
-    monkeypatch.delenv("GNS_SHARE_SYM", raising=False)
     X = gen.gaussian_bucket(24, 1024, 2048, seed=901)
     grouped = run_gpu(gns, X)
     for g in (0, 23):

@@ -202,3 +202,25 @@ def test_normuon_eps_outside_the_square_root():
     scale = np.linalg.norm(U, axis=1) / np.linalg.norm(O, axis=1)
     want = (np.sqrt(v[1]) + eps) / (np.sqrt(v[0]) + eps)
     assert np.isclose(scale[0] / scale[1], want, rtol=1e-14)
+
+
+@pytest.mark.parametrize("shape", [(96, 200), (256, 1024)])
+def test_sr_update_check_separates_rounding_noise_from_error(shape):
+    """The GPU tests judge a stochastically rounded update with
+    gpu_helpers.sr_update_error, which subtracts the expected rounding noise.
+    Pinned here on the oracle alone: an update computed from an
+    orthogonalized matrix with a planted relative error of 0, 2 or 3 % passes
+    and its estimated error is the planted one; 4 and 5 % fail."""
+    from gpu_helpers import sr_update_error
+    r, c = shape
+    rng = np.random.default_rng(r * c)
+    w = MU.f32_to_bf16_rne_bits((0.02 * rng.standard_normal((r, c))).astype(np.float32))
+    o = rng.standard_normal((r, c)) / np.sqrt(max(r, c))
+    s = MU.update_scale(r, c)
+    for planted, expect in ((0.0, True), (0.02, True), (0.03, True), (0.04, False), (0.05, False)):
+        d = rng.standard_normal((r, c))
+        d *= planted * np.linalg.norm(o) / np.linalg.norm(d)
+        got = MU.muon_update_bf16(w, (o + d).astype(np.float32), 0.02, 0.01, s, seed=7, step=3)
+        ok, est, _ = sr_update_error(got, w, o, 0.02, 0.01, s)
+        assert ok == expect, (planted, est)
+        assert abs(est - planted) < 2e-3, (planted, est)
