@@ -213,11 +213,17 @@ def cpu_threads():
     return os.cpu_count()
 
 
-def rank_seed(rank):
-    """Seed of a rank's bucket: every rank orthogonalizes its own independent
-    bucket (the matrices of a bucket are independent problems), so ranks
-    share no data and exchange nothing but timings."""
-    return 2000 + rank
+SEED = 2000
+
+
+def rank_chunk(rank, world):
+    """(start, count) of this rank's matrices: the job orthogonalizes one
+    bucket of G x world matrices, split into contiguous per-rank chunks
+    (newton_schulz_gram_gb300.partition; the matrices are independent, so
+    ranks share no data and exchange nothing but timings). G per rank is
+    fixed: weak scaling."""
+    from newton_schulz_gram_gb300.partition import partition
+    return partition(G * world, world, rank)
 
 
 def max_over_ranks(value, dist, device):
@@ -236,9 +242,10 @@ def job_throughput(units_per_rank, world, seconds):
     return units_per_rank * world / seconds
 
 
-def make_bucket(seed):
+def make_bucket(rank=0, world=1):
     from inputs import generators as gen
-    return gen.gaussian_bucket(G, R, C, seed)
+    start, count = rank_chunk(rank, world)
+    return gen.gaussian_bucket(count, R, C, SEED, first=start)
 
 
 def run_reference(args, rank, world):
@@ -246,7 +253,7 @@ def run_reference(args, rank, world):
     the bucket in fp64 on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    bucket = make_bucket(rank_seed(0))
+    bucket = make_bucket()
     import numpy as np
     from oracle import gram_ns
     for i in range(args.warmup):
@@ -389,7 +396,7 @@ def single_thread_oracle(budget_s=10.0):
             "while n < 3:\n"
             "    gram_ns.orthogonalize(X[n].astype(np.float64), %d, None, %d); n += 1\n"
             "    if time.perf_counter() - t0 > %f: break\n"
-            "print(n, time.perf_counter() - t0)") % (ROOT, R, C, rank_seed(0), T_STEPS, RESTART, budget_s)
+            "print(n, time.perf_counter() - t0)") % (ROOT, R, C, SEED, T_STEPS, RESTART, budget_s)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     try:
         r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
@@ -444,7 +451,7 @@ def main():
     torch.cuda.set_device(dev)
     gns.load()
 
-    bucket = make_bucket(rank_seed(rank))
+    bucket = make_bucket(rank, world)
     host = torch.from_numpy(bucket).pin_memory()
     x = host.to(dev, non_blocking=False)
     stream = torch.cuda.current_stream(dev)

@@ -143,8 +143,9 @@ typedef struct {
  * with the update in fp32 (decay = 1 - lr*wd, step = lr*s,
  * w' = decay*w - step*o, each rounded once) and a stochastically rounded
  * bf16 write-back keyed by (seed, step, base_index + element index)
- * (Philox4x32-10; element i uses the low 16 bits of output word (g & 3) of
- * the block g >> 2, g = base_index + i).
+ * (Philox4x32-10: one output serves the block g >> 3 of eight global indices,
+ * element g = base_index + i taking the 16-bit half (g & 1), low first, of
+ * output word (g & 7) >> 1).
  *
  *   params    n tensors, bf16 weights, updated in place.
  *   grads     n tensors, bf16 gradients (same shapes), read.

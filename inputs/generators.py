@@ -133,10 +133,13 @@ def moe_matrix(kind, rows, cols, seed, index):
     raise ValueError(kind)
 
 
-def gaussian_bucket(G, rows, cols, seed):
+def gaussian_bucket(G, rows, cols, seed, first=0):
+    """Matrices first .. first + G - 1 of the seeded Gaussian bucket (each
+    from its own (seed, index) generator, so any chunk of a bucket is the
+    same data as in the whole bucket)."""
     out = np.empty((G, rows, cols), dtype=np.float32)
     for g in range(G):
-        out[g] = gaussian(rows, cols, seed, g)
+        out[g] = gaussian(rows, cols, seed, first + g)
     return out
 
 

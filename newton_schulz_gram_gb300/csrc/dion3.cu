@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(1024) gather_cols_kernel(MatrixSet Ms, int R, 
 
 // Every element of W[g] (R x C): o from O (row or column p of the selection,
 // or 0), the fused update with stochastic rounding, and error feedback on
-// the selected part of M. One thread per group of 4 global indices.
+// the selected part of M. One thread per block of 8 global indices (one
+// Philox output).
 __global__ void __launch_bounds__(kThreads) update_kernel(MatrixSet Ws, MatrixSet Ms, const __half* O, long long ld_o,
                                                           long long stride_o, const int* pos, int nsel,
                                                           const long long* base_dev, int R, int C, int cols,
@@ -176,17 +177,17 @@ __global__ void __launch_bounds__(kThreads) update_kernel(MatrixSet Ws, MatrixSe
     const long long numel = static_cast<long long>(R) * C;
     const float decay = __fsub_rn(1.0f, __fmul_rn(lr, wd));
     const float stepv = __fmul_rn(lr, scale);
-    const long long blk_first = base >> 2;
-    const long long nblk = ((base + numel - 1) >> 2) - blk_first + 1;
+    const long long blk_first = base >> 3;
+    const long long nblk = ((base + numel - 1) >> 3) - blk_first + 1;
     for (long long t = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; t < nblk;
          t += static_cast<long long>(gridDim.x) * kThreads) {
         const long long blk = blk_first + t;
         uint32_t c[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(static_cast<unsigned long long>(blk) >> 32),
                          s0, s1};
         philox4x32_10(c, k0, k1);
-        const long long i0 = blk * 4 - base;
+        const long long i0 = blk * 8 - base;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 8; ++e) {
             const long long i = i0 + e;
             if (i < 0 || i >= numel) continue;
             const int r = static_cast<int>(i / C), col = static_cast<int>(i - static_cast<long long>(r) * C);
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(MatrixSet Ws, MatrixSe
             }
             const float w = __uint_as_float(static_cast<uint32_t>(W[i]) << 16);
             const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
-            W[i] = sr_bf16(wn, c[e] & 0xFFFFu);
+            W[i] = sr_bf16(wn, sr_draw(c, e));
         }
     }
 }
@@ -250,8 +251,8 @@ int launch_dion3_update(const MatrixSet& W, const MatrixSet& M, const void* O, l
                         const int* pos, int nsel, const long long* base_dev, int count, int R, int C, bool cols,
                         float lr, float wd, float scale, float mu, uint64_t seed, uint64_t step, cudaStream_t s) {
     if (count <= 0) return cudaSuccess;
-    const long long groups = static_cast<long long>(R) * C / 4 + 2;
-    return launch_pdl(update_kernel, dim3(blocks_for(groups, kThreads * 4), count), dim3(kThreads), 0, s, W, M,
+    const long long groups = static_cast<long long>(R) * C / 8 + 2;
+    return launch_pdl(update_kernel, dim3(blocks_for(groups, kThreads * 2), count), dim3(kThreads), 0, s, W, M,
                       static_cast<const __half*>(O), ld_o, stride_o, pos, nsel, base_dev, R, C, cols ? 1 : 0, lr, wd,
                       scale, mu, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32),
                       static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32));

@@ -1,18 +1,15 @@
-// HBM-bound kernels around the GEMM core: the Frobenius norm, the
-// scale / cast / transpose to fp16, and the two Muon elementwise passes.
+// HBM-bound kernels around the GEMM core: the Muon elementwise passes (the
+// standalone momentum and update kernels), the NorMuon statistics, the copy
+// of unaligned outputs and the bounded-wait check. (The norm, scale and fp16
+// cast of the inputs run as the first items of the GEMM program.)
 //
 // Arithmetic contracts (shared with nothing else; restated from the pages):
-// * Norm (Dion3 Algorithm 3, line 2, with the App. B.2.2 safety factor):
-//   s = 2^k / (1.05 (||X||_F + 1e-7)). The 2^k is an exact power-of-two
-//   prescale of the fp16 copy, undone by the GEMM epilogues.
-//   The sum of squares is deterministic: each matrix is cut into a number of
-//   chunks that depends only on its size, each chunk summed in a fixed order.
 // * Momentum (Dion3 Eq. 1): M <- mu M + G, fp32, two roundings.
 // * Update (Dion3 §6 "Weight Update"; Muon kernel card): decay = 1 - lr wd,
 //   step = lr s, w' = decay w - step o, each fp32 operation rounded once,
 //   then stochastic rounding to bf16 with Philox4x32-10 (Salmon et al.,
-//   SC'11) keyed by (seed, step) and counter (g >> 2, step), g = base + i;
-//   element g uses the low 16 bits of output word g & 3.
+//   SC'11) keyed by (seed, step) and counter (g >> 3, step), g = base + i;
+//   element g uses 16-bit half (g & 1) of output word (g & 7) >> 1.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -451,9 +448,9 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(MatrixSet Ms, Matrix
                                  threadIdx.x);
 }
 
-// One thread per group of 4 global indices g = 4 blk .. 4 blk + 3. With
-// row_step (NorMuon), row r of matrix g takes the step row_step[g R + r]
-// instead of lr * scale.
+// One thread per block of 8 global indices g = 8 blk .. 8 blk + 7 (one
+// Philox output). With row_step (NorMuon), row r of matrix g takes the step
+// row_step[g R + r] instead of lr * scale.
 __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, MatrixSet Os, long long ld_o,
                                                                const long long* base_dev, long long base_scalar,
                                                                int R, int C, float lr, float wd, float scale,
@@ -470,40 +467,43 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
     const float step_all = __fmul_rn(lr, scale);
     const float* rs = row_step ? row_step + static_cast<long long>(g) * R : nullptr;
     // Blocks of the global index space that overlap [base, base + numel).
-    const long long blk_first = base >> 2;
-    const long long blk_last = (base + numel - 1) >> 2;
+    const long long blk_first = base >> 3;
+    const long long blk_last = (base + numel - 1) >> 3;
     const long long nblk = blk_last - blk_first + 1;
-    const bool fast = ((base & 3) == 0) && (C % 4 == 0) && (ld_o % 4 == 0) &&
-                      ((reinterpret_cast<uintptr_t>(W) & 7) == 0) && ((reinterpret_cast<uintptr_t>(O) & 7) == 0);
+    const bool fast = ((base & 7) == 0) && (C % 8 == 0) && (ld_o % 8 == 0) &&
+                      ((reinterpret_cast<uintptr_t>(W) & 15) == 0) && ((reinterpret_cast<uintptr_t>(O) & 15) == 0);
     for (long long t = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; t < nblk;
          t += static_cast<long long>(gridDim.x) * kThreads) {
         const long long blk = blk_first + t;
         uint32_t c[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(static_cast<unsigned long long>(blk) >> 32),
                          s0, s1};
         philox4x32_10(c, k0, k1);
-        const long long i0 = blk * 4 - base;  // local index of global index 4 blk
+        const long long i0 = blk * 8 - base;  // local index of global index 8 blk
         if (fast) {
+            // Eight elements of one row: 16-byte loads and store.
             const long long r = i0 / C, col = i0 - r * C;
             const float stepv = rs ? rs[r] : step_all;
-            const uint2 wraw = *reinterpret_cast<const uint2*>(W + i0);
-            const uint2 oraw = *reinterpret_cast<const uint2*>(O + r * ld_o + col);
+            const uint4 wraw = *reinterpret_cast<const uint4*>(W + i0);
+            const uint4 oraw = *reinterpret_cast<const uint4*>(O + r * ld_o + col);
             const uint16_t* wv = reinterpret_cast<const uint16_t*>(&wraw);
             const __half* ov = reinterpret_cast<const __half*>(&oraw);
-            uint16_t outv[4];
+            uint32_t outv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float w = __uint_as_float(static_cast<uint32_t>(wv[e]) << 16);
-                const float o = __half2float(ov[e]);
-                const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
-                outv[e] = sr_bf16(wn, c[e] & 0xFFFFu);
+            for (int e = 0; e < 8; e += 2) {
+                uint32_t pair = 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float w = __uint_as_float(static_cast<uint32_t>(wv[e + h]) << 16);
+                    const float o = __half2float(ov[e + h]);
+                    const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
+                    pair |= static_cast<uint32_t>(sr_bf16(wn, sr_draw(c, e + h))) << (16 * h);
+                }
+                outv[e >> 1] = pair;
             }
-            uint2 packed;
-            packed.x = static_cast<uint32_t>(outv[0]) | (static_cast<uint32_t>(outv[1]) << 16);
-            packed.y = static_cast<uint32_t>(outv[2]) | (static_cast<uint32_t>(outv[3]) << 16);
-            *reinterpret_cast<uint2*>(W + i0) = packed;
+            *reinterpret_cast<uint4*>(W + i0) = make_uint4(outv[0], outv[1], outv[2], outv[3]);
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 8; ++e) {
                 const long long i = i0 + e;
                 if (i < 0 || i >= numel) continue;
                 const long long r = i / C, col = i - r * C;
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
                 const float w = __uint_as_float(static_cast<uint32_t>(W[i]) << 16);
                 const float o = __half2float(O[r * ld_o + col]);
                 const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
-                W[i] = sr_bf16(wn, c[e] & 0xFFFFu);
+                W[i] = sr_bf16(wn, sr_draw(c, e));
             }
         }
     }
@@ -653,8 +653,7 @@ int launch_norm_cast(const NormCastJob& job, int num_sms, cudaStream_t s) {
     const long long total = static_cast<long long>(job.G) * 2 * a.nparts;
     if (total > (1LL << 30)) return cudaErrorInvalidValue;
     a.total = static_cast<int>(total);
-    cudaError_t e = cudaMemsetAsync(job.queue, 0, sizeof(int) * (1 + static_cast<size_t>(job.G)), s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     static int per_sm[2] = {0, 0};
     int& occ = per_sm[momentum ? 1 : 0];
     if (occ == 0) {
@@ -707,8 +706,8 @@ int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o, c
                        long long base_scalar, int count, int R, int C, float lr, float wd, float scale,
                        uint64_t seed, uint64_t step, cudaStream_t s, const float* row_step) {
     if (count <= 0 || static_cast<long long>(R) * C <= 0) return cudaSuccess;
-    const long long groups = static_cast<long long>(R) * C / 4 + 2;
-    return launch_pdl(muon_update_kernel, dim3(grid_for(groups, kThreads * 4), count), dim3(kThreads), s, W, O,
+    const long long groups = static_cast<long long>(R) * C / 8 + 2;
+    return launch_pdl(muon_update_kernel, dim3(grid_for(groups, kThreads * 2), count), dim3(kThreads), s, W, O,
                       ld_o, base_dev, base_scalar, R, C, lr, wd, scale, row_step, static_cast<uint32_t>(seed),
                       static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(step),
                       static_cast<uint32_t>(step >> 32));

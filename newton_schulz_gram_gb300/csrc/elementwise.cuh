@@ -4,43 +4,18 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "gemm.cuh"
 #include "ptx.cuh"
 
 namespace gns {
-
-// A set of G matrices: either contiguous (base + g * stride) or a device
-// array of per-matrix pointers (ptrs != nullptr).
-struct MatrixSet {
-    const void* base;
-    long long stride;       // elements between matrices when contiguous
-    const void* const* ptrs;
-};
-
-// The Frobenius norm is summed in parts of norm_part_len(numel) elements
-// (the last one shorter), norm_parts(numel) per matrix: a function of the
-// matrix size only, so a matrix's scale never depends on its bucket.
-constexpr long long kNormPartElems = 16384;
-constexpr int kMaxNormParts = 8192;
-
-__host__ __device__ inline long long norm_part_len(long long numel) {
-    const long long even = (numel + kMaxNormParts - 1) / kMaxNormParts;
-    const long long len = (even + 3) & ~3LL;
-    return len > kNormPartElems ? len : kNormPartElems;
-}
-
-__host__ __device__ inline int norm_parts(long long numel) {
-    const long long len = norm_part_len(numel);
-    const long long p = (numel + len - 1) / len;
-    return static_cast<int>(p < 1 ? 1 : p);
-}
 
 // Norm, scale and cast of a bucket of G fp32 R x C matrices in one pass:
 //   [momentum only] M[g] <- mu M[g] + float(grads[g]) (in place, fp32),
 //   scale_g = 2^k_exp / (1.05 (||x_g||_F + 1e-7)),
 //   out[g] (R x C, row stride ld_out, a multiple of 8) = fp16(scale_g x_g).
-// partial holds G * norm_parts(R C) floats and queue 1 + G ints (zeroed
-// here, stream-ordered). A non-finite norm raises the
-// non-finite error word.
+// partial holds G * norm_parts(R C) floats and queue 1 + G ints, which the
+// caller zeroes (stream-ordered) before the launch. A non-finite norm raises
+// the non-finite error word.
 struct NormCastJob {
     MatrixSet in;     // fp32 input matrices, or the momentum M (updated in place)
     MatrixSet grads;  // bf16 gradients; base and ptrs both null: no momentum update

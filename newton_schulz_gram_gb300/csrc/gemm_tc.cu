@@ -32,6 +32,8 @@
 // are staged as two 16-column halves).
 #include <cstdio>
 
+#include <cuda_bf16.h>
+
 #include "gemm.cuh"
 #include "philox.cuh"
 #include "ptx.cuh"
@@ -42,7 +44,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 static_assert(sizeof(GemmProgram) <= 32764, "kernel parameter block too large");
-constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 
 // Per-warp epilogue shared memory: three 2 KB slots of 32 rows x 64 bytes
@@ -72,31 +73,31 @@ struct Cfg<256, 2> {
     static constexpr int STAGES = 5;
 };
 
-// Tile-walk tables, copied from the kernel parameters into shared memory at
-// start: every role decodes every tile it visits, and parameter-space loads
-// with a tile-dependent index are slow under load.
+// Tables copied from the kernel parameters into shared memory at start: the
+// item-list builder decodes every item through them, and the roles read a
+// problem's fields per tile (parameter-space loads with a tile-dependent
+// index are slow under load).
 struct CtlPhase {
-    int tile_begin, tiles_per_matrix, prob_begin, reverse, wait_tiles;
+    int item_begin, tiles_per_matrix, prob_begin, wait;
 };
 struct CtlProb {
-    int tiles_per_matrix, tiles_n, tiles_n_walk, flags, K, tiles_m;
+    int tiles_per_matrix, tiles_n, flags, K, tiles_m;
     int mA, mB, mAt, mBt, mC;
 };
 constexpr int kCtlBytes = kMaxPhases * static_cast<int>(sizeof(CtlPhase)) + kMaxProblems * static_cast<int>(sizeof(CtlProb));
+// Shared words of the epilogue group: the per-warp values of a reduction,
+// a broadcast flag and the list lengths.
+constexpr int kEpiWords = 16;
 __host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 5 + 2 * kEpiWarps; }
 
 template <int BN, int CG>
 constexpr int smem_bytes() {
     return 1024 + Cfg<BN, CG>::STAGES * (BM * BK * 2 + (BN / CG) * BK * 2) + kEpiWarps * SBUF +
-           kNumBars(Cfg<BN, CG>::STAGES) * 8 + 16 + kCtlBytes;
+           kNumBars(Cfg<BN, CG>::STAGES) * 8 + 16 + kCtlBytes + 4 * kEpiWords;
 }
 static_assert(smem_bytes<256, 2>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<128, 1>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<256, 1>() <= 232448, "shared memory budget");
-
-struct TileInfo {
-    int p, g, m0, n0, s;  // problem, matrix, tile origin, phase
-};
 
 // Column blocks a symmetric row block of height tm touches: j * bn <= tm i + tm - 1.
 __host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int tiles_n) {
@@ -104,111 +105,20 @@ __host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int
     return c < tiles_n ? c : tiles_n;
 }
 
-// Decodes program tiles for one role. A role visits the tiles first,
-// first + step, first + 2 step, ...; phases change only a few dozen times per
-// program. The walker keeps the current phase and its (at most two) problems
-// in registers, reads the shared-memory tables only when the phase changes,
-// and within a phase advances the (matrix, tile) position by the fixed
-// stride instead of dividing: the decode runs on a single thread between
-// k-blocks, where every dependent instruction counts.
+__host__ __device__ __forceinline__ int item_kind(const ProgItem& it) { return it.meta & 3; }
+__host__ __device__ __forceinline__ int item_prob(const ProgItem& it) { return (it.meta >> 2) & 63; }
+__host__ __device__ __forceinline__ int item_matrix(const ProgItem& it) { return static_cast<int>(static_cast<unsigned>(it.meta) >> 8); }
+__host__ __device__ __forceinline__ ProgItem make_item(int kind, int p, int g, int wait, int m0, int n0) {
+    return ProgItem{kind | (p << 2) | (g << 8), wait, m0, n0};
+}
+
+// Tile t (0-based, in walk order) of matrix g in phase `s`: the problem it
+// belongs to and its origin. Symmetric products list the lower-triangle tiles
+// row by row; other products walk row by row, or column by column with
+// kFlagColWalk (the tiles that share a B column block run together).
 template <int BN, int CG>
-struct TileWalker {
-    static constexpr int TM = BM * CG;
-    const CtlPhase* cph;
-    const CtlProb* cpb;
-    int nphase, G, step;
-    int s = -1, next_begin = 0;  // current phase and the first tile of the next one
-    CtlPhase ph{};
-    CtlProb pb[2]{};             // the phase's problems
-    float inv_wn[2]{};           // 1 / (tiles walked per row, or per column) of each problem
-    int lg = 0, lt = 0;          // position of the last tile: matrix slot, tile within the matrix
-    int sq = 0, sr = 0;          // step = sq tiles_per_matrix + sr
-    int cur = 0;                 // which of pb[] the last decoded tile belongs to
-
-    __device__ __forceinline__ TileWalker(const CtlPhase* a, const CtlProb* b, int np, int g, int stp)
-        : cph(a), cpb(b), nphase(np), G(g), step(stp) {}
-
-    __device__ __forceinline__ const CtlProb& prob() const { return cur ? pb[1] : pb[0]; }
-
-    // Decodes `tile`, which must be the first tile or the previous one + step.
-    __device__ __forceinline__ TileInfo decode(int tile) {
-        if (tile >= next_begin) {
-            while (s + 1 < nphase && tile >= cph[s + 1].tile_begin) ++s;
-            ph = cph[s];
-            next_begin = s + 1 < nphase ? cph[s + 1].tile_begin : 0x7fffffff;
-            pb[0] = cpb[ph.prob_begin];
-            if (ph.tiles_per_matrix > pb[0].tiles_per_matrix) pb[1] = cpb[ph.prob_begin + 1];
-            for (int q = 0; q < 2; ++q) {
-                const int w = (pb[q].flags & kFlagColWalk) ? pb[q].tiles_m : pb[q].tiles_n_walk;
-                inv_wn[q] = 1.0f / static_cast<float>(w > 0 ? w : 1);
-            }
-            const int local = tile - ph.tile_begin;
-            lg = local / ph.tiles_per_matrix;
-            lt = local - lg * ph.tiles_per_matrix;
-            sq = step / ph.tiles_per_matrix;
-            sr = step - sq * ph.tiles_per_matrix;
-        } else {
-            lt += sr;
-            lg += sq;
-            if (lt >= ph.tiles_per_matrix) {
-                lt -= ph.tiles_per_matrix;
-                ++lg;
-            }
-        }
-        const int g = ph.reverse ? G - 1 - lg : lg;
-        int t = lt;
-        cur = t >= pb[0].tiles_per_matrix ? 1 : 0;
-        if (cur) t -= pb[0].tiles_per_matrix;
-        const CtlProb& pr = prob();
-        const int flags = pr.flags;
-        int i, j;
-        // Tiles past the real ones (padding) decode to out-of-range tiles: their
-        // loads read zeros and their epilogue writes nothing.
-        if ((flags & kFlagSym) && TM == BN) {
-            // Square tiles: row block i holds i + 1 tiles, i (i + 1) / 2 before it.
-            i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
-            if (i * (i + 1) / 2 > t) --i;
-            if ((i + 1) * (i + 2) / 2 <= t) ++i;
-            j = t - i * (i + 1) / 2;
-        } else if (flags & kFlagSym) {
-            int acc = 0;
-            i = 0;
-            while (true) {
-                const int cnt = sym_row_tiles(i, TM, BN, pr.tiles_n);
-                if (t < acc + cnt) break;
-                acc += cnt;
-                ++i;
-            }
-            j = t - acc;
-        } else if (flags & kFlagColWalk) {
-            const int wm = pr.tiles_m;
-            j = static_cast<int>(static_cast<float>(t) * (cur ? inv_wn[1] : inv_wn[0]));
-            if (j * wm > t) --j;
-            if ((j + 1) * wm <= t) ++j;
-            i = t - j * wm;
-        } else {
-            const int wn = pr.tiles_n_walk;
-            i = static_cast<int>(static_cast<float>(t) * (cur ? inv_wn[1] : inv_wn[0]));
-            if (i * wn > t) --i;
-            if ((i + 1) * wn <= t) ++i;
-            j = t - i * wn;
-        }
-        return TileInfo{ph.prob_begin + cur, g, i * TM, j * BN, s};
-    }
-};
-
-// The same decode straight from the shared-memory tables, resuming the phase
-// search at `s` (used where registers are scarce).
-template <int BN, int CG>
-__device__ __forceinline__ TileInfo decode_tile(const CtlPhase* cph, const CtlProb* cpb, int nphase, int G, int tile,
-                                                int& s) {
+__host__ __device__ ProgItem decode_tile(const CtlPhase& ph, const CtlProb* cpb, int g, int t) {
     constexpr int TM = BM * CG;
-    while (s + 1 < nphase && tile >= cph[s + 1].tile_begin) ++s;
-    const CtlPhase ph = cph[s];
-    const int local = tile - ph.tile_begin;
-    int g = local / ph.tiles_per_matrix;
-    int t = local - g * ph.tiles_per_matrix;
-    if (ph.reverse) g = G - 1 - g;
     int p = ph.prob_begin;
     while (t >= cpb[p].tiles_per_matrix) {
         t -= cpb[p].tiles_per_matrix;
@@ -217,31 +127,60 @@ __device__ __forceinline__ TileInfo decode_tile(const CtlPhase* cph, const CtlPr
     const int flags = cpb[p].flags;
     int i, j;
     if ((flags & kFlagSym) && TM == BN) {
+        // Square tiles: row block i holds i + 1 tiles, i (i + 1) / 2 before it.
         i = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
         while (i * (i + 1) / 2 > t) --i;
         while ((i + 1) * (i + 2) / 2 <= t) ++i;
         j = t - i * (i + 1) / 2;
     } else if (flags & kFlagSym) {
-        const int tiles_n = cpb[p].tiles_n;
         int acc = 0;
         i = 0;
         while (true) {
-            const int cnt = sym_row_tiles(i, TM, BN, tiles_n);
+            const int cnt = sym_row_tiles(i, TM, BN, cpb[p].tiles_n);
             if (t < acc + cnt) break;
             acc += cnt;
             ++i;
         }
         j = t - acc;
     } else if (flags & kFlagColWalk) {
-        const int wm = cpb[p].tiles_m;
-        j = t / wm;
-        i = t - j * wm;
+        j = t / cpb[p].tiles_m;
+        i = t - j * cpb[p].tiles_m;
     } else {
-        const int wn = cpb[p].tiles_n_walk;
-        i = t / wn;
-        j = t - i * wn;
+        i = t / cpb[p].tiles_n;
+        j = t - i * cpb[p].tiles_n;
     }
-    return TileInfo{p, g, i * TM, j * BN, s};
+    return make_item(kItemTile, p, g, ph.wait, i * TM, j * BN);
+}
+
+// Item w of the program's list. With prep items (q norm and q cast items per
+// matrix), the list starts with G + 1 rounds: round r holds the norm items of
+// matrix r (r < G), then the cast items of matrix r - 1 (1 <= r <= G). The
+// phases' tiles follow, phase by phase, matrix by matrix.
+template <int BN, int CG>
+__host__ __device__ ProgItem decode_item(const CtlPhase* cph, const CtlProb* cpb, int nphase, int G, int q, int w) {
+    constexpr int spi = kEpiWarps * CG;  // counter signals per item
+    if (q > 0 && w < 2LL * q * G) {
+        // Rounds 1 .. G - 1 hold 2q items; round 0 holds q, round G holds q.
+        int r, o;
+        if (w < q) {
+            r = 0;
+            o = w;
+        } else {
+            r = 1 + (w - q) / (2 * q);
+            o = (w - q) - (r - 1) * 2 * q;
+        }
+        if (r < G) {
+            if (o < q) return make_item(kItemNorm, 0, r, 0, o, 0);
+            o -= q;
+        }
+        // Casts wait for every norm item of the matrix and its scale.
+        return make_item(kItemCast, 0, r - 1, q * spi + 1, o, 0);
+    }
+    int s = 0;
+    while (s + 1 < nphase && w >= cph[s + 1].item_begin) ++s;
+    const int local = w - cph[s].item_begin;
+    const int g = local / cph[s].tiles_per_matrix;
+    return decode_tile<BN, CG>(cph[s], cpb, g, local - g * cph[s].tiles_per_matrix);
 }
 
 // An MN-major operand tile is staged as 64-wide M/N blocks of 64 K rows
@@ -371,6 +310,43 @@ __device__ __forceinline__ void store_rows64(uint32_t stg, const OutView& o, int
     }
 }
 
+// 32 bytes to global memory in one store (sm_100 and later).
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
+// An output whose rows (and matrices) start on 32-byte boundaries takes the
+// direct path below for full-width blocks.
+__device__ __forceinline__ bool out_direct(const OutView& o, int es) {
+    return (reinterpret_cast<uintptr_t>(o.p) & 31) == 0 && ((o.ld * es) & 31) == 0 && ((o.stride * es) & 31) == 0;
+}
+
+// Row `row` of a 32 x 32 block, columns c0 .. c0 + 31, written straight from
+// the lane's registers (no shared-memory staging): 32 fp16 values (64 bytes)
+// as two 32-byte stores, or 32 fp32 values as four.
+__device__ __forceinline__ void direct_row(const OutView& o, int g, int row, int c0, const float (&v)[32], bool f32) {
+    const long long idx = static_cast<long long>(g) * o.stride + static_cast<long long>(row) * o.ld + c0;
+    if (f32) {
+        float* p = static_cast<float*>(o.p) + idx;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            st_global_v8(p + 8 * k, __float_as_uint(v[8 * k + 0]), __float_as_uint(v[8 * k + 1]),
+                         __float_as_uint(v[8 * k + 2]), __float_as_uint(v[8 * k + 3]), __float_as_uint(v[8 * k + 4]),
+                         __float_as_uint(v[8 * k + 5]), __float_as_uint(v[8 * k + 6]), __float_as_uint(v[8 * k + 7]));
+    } else {
+        __half* p = static_cast<__half*>(o.p) + idx;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            st_global_v8(p + 16 * k, pack_half2(v[16 * k + 0], v[16 * k + 1]), pack_half2(v[16 * k + 2], v[16 * k + 3]),
+                         pack_half2(v[16 * k + 4], v[16 * k + 5]), pack_half2(v[16 * k + 6], v[16 * k + 7]),
+                         pack_half2(v[16 * k + 8], v[16 * k + 9]), pack_half2(v[16 * k + 10], v[16 * k + 11]),
+                         pack_half2(v[16 * k + 12], v[16 * k + 13]), pack_half2(v[16 * k + 14], v[16 * k + 15]));
+    }
+}
+
 // The rarer epilogue paths.
 // A 32 x 32 fp32 block, staged and stored as two 16-column halves (inline:
 // the values are a register array, which a call would move to local memory).
@@ -417,7 +393,7 @@ __device__ __forceinline__ void muon_update_row(const GemmProblem& pr, int g, in
     };
     // Register arrays only: every index below is a compile-time constant
     // (a runtime index would move v to local memory for every tile).
-    if (ncol == 32 && (g0 & 3) == 0 && (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
+    if (ncol == 32 && (g0 & 7) == 0 && (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
         uint32_t wv[16];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -427,17 +403,18 @@ __device__ __forceinline__ void muon_update_row(const GemmProblem& pr, int g, in
             wv[4 * k + 2] = x.z;
             wv[4 * k + 3] = x.w;
         }
+        // Four blocks of eight global indices, one Philox output each.
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const unsigned long long blk = (g0 >> 2) + b;
+        for (int b = 0; b < 4; ++b) {
+            const unsigned long long blk = (g0 >> 3) + b;
             uint32_t c[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), mf.step_lo, mf.step_hi};
             philox4x32_10(c, mf.seed_lo, mf.seed_hi);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t pair = wv[2 * b + h];
-                const uint32_t lo = upd(static_cast<uint16_t>(pair & 0xFFFFu), v[4 * b + 2 * h], c[2 * h]);
-                const uint32_t hi = upd(static_cast<uint16_t>(pair >> 16), v[4 * b + 2 * h + 1], c[2 * h + 1]);
-                wv[2 * b + h] = lo | (hi << 16);
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t pair = wv[4 * b + h];
+                const uint32_t lo = upd(static_cast<uint16_t>(pair & 0xFFFFu), v[8 * b + 2 * h], sr_draw(c, 2 * h));
+                const uint32_t hi = upd(static_cast<uint16_t>(pair >> 16), v[8 * b + 2 * h + 1], sr_draw(c, 2 * h + 1));
+                wv[4 * b + h] = lo | (hi << 16);
             }
         }
 #pragma unroll
@@ -445,24 +422,22 @@ __device__ __forceinline__ void muon_update_row(const GemmProblem& pr, int g, in
             reinterpret_cast<uint4*>(wp)[k] = make_uint4(wv[4 * k + 0], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
     } else {
         unsigned long long cur = ~0ULL;
-        uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+        uint32_t c[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             if (j < ncol) {
                 const unsigned long long gi = g0 + j;
-                if ((gi >> 2) != cur) {
-                    cur = gi >> 2;
-                    uint32_t c[4] = {static_cast<uint32_t>(cur), static_cast<uint32_t>(cur >> 32), mf.step_lo,
-                                     mf.step_hi};
+                if ((gi >> 3) != cur) {
+                    cur = gi >> 3;
+                    c[0] = static_cast<uint32_t>(cur);
+                    c[1] = static_cast<uint32_t>(cur >> 32);
+                    c[2] = mf.step_lo;
+                    c[3] = mf.step_hi;
                     philox4x32_10(c, mf.seed_lo, mf.seed_hi);
-                    c0 = c[0];
-                    c1 = c[1];
-                    c2 = c[2];
-                    c3 = c[3];
                 }
-                const uint32_t e = static_cast<uint32_t>(gi & 3);
-                const uint32_t u = e == 0 ? c0 : (e == 1 ? c1 : (e == 2 ? c2 : c3));
-                wp[j] = upd(wp[j], v[j], u);
+                const int e = static_cast<int>(gi & 7);
+                const uint32_t u = (e >> 1) == 0 ? c[0] : ((e >> 1) == 1 ? c[1] : ((e >> 1) == 2 ? c[2] : c[3]));
+                wp[j] = upd(wp[j], v[j], (u >> (16 * (e & 1))) & 0xFFFFu);
             }
         }
     }
@@ -474,6 +449,195 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer() - t0 > limit_ns) break;
     }
+}
+
+// ------------------------------------------------------------ prep items
+//
+// Run by each epilogue warp on its own, with no barrier among the warps:
+// norm and cast item i of matrix g cover part i * CG + rank (one part per
+// CTA of the pair), and warp w of a CTA owns slice w of every 16384-element
+// chunk of the part: 2048 elements, lane l taking the float4 groups
+// l + 32 u (u = 0 .. 15). Every sum runs in a fixed order, so a matrix's
+// scale depends on its size only (not on the bucket or the tile shape).
+
+constexpr int kSliceElems = static_cast<int>(kNormPartElems / kEpiWarps);  // 2048
+constexpr int kSliceVec = kSliceElems / (4 * 32);                           // float4 per lane: 16
+static_assert(kSliceVec * 4 * 32 * kEpiWarps == kNormPartElems, "a chunk is kEpiWarps slices");
+
+__device__ __forceinline__ float* prep_f32(const MatrixSet& s, int g) {
+    return s.ptrs ? static_cast<float*>(const_cast<void*>(s.ptrs[g]))
+                  : static_cast<float*>(const_cast<void*>(s.base)) + static_cast<long long>(g) * s.stride;
+}
+
+__device__ __forceinline__ const __nv_bfloat16* prep_bf16(const MatrixSet& s, int g) {
+    return s.ptrs ? static_cast<const __nv_bfloat16*>(s.ptrs[g])
+                  : static_cast<const __nv_bfloat16*>(s.base) + static_cast<long long>(g) * s.stride;
+}
+
+__device__ __forceinline__ float4 momentum4(float4 m, uint2 graw, float mu) {
+    const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&graw);
+    const float2 g01 = __bfloat1622float2(gb[0]);
+    const float2 g23 = __bfloat1622float2(gb[1]);
+    m.x = __fadd_rn(__fmul_rn(mu, m.x), g01.x);
+    m.y = __fadd_rn(__fmul_rn(mu, m.y), g01.y);
+    m.z = __fadd_rn(__fmul_rn(mu, m.z), g23.x);
+    m.w = __fadd_rn(__fmul_rn(mu, m.w), g23.y);
+    return m;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Norm item, one warp: the sum of squares of its slices of the part (after
+// the momentum update, which it stores) into partial[g][part * kEpiWarps + w];
+// then the warp's signal. The warp whose signal completes the matrix's norm
+// items (counter value q * spi - 1 before it) sums all of the matrix's
+// partials in a fixed order and publishes scale[g] with one more signal.
+static __device__ __noinline__ void prep_norm(const PrepDesc& d, int* counter, int done_target, const DevStatus& st,
+                                              int g, int part, int w, int lane) {
+    float s = 0.0f;
+    if (part < d.nparts) {
+        float* x = prep_f32(d.in, g);
+        const __nv_bfloat16* gr = d.momentum ? prep_bf16(d.grads, g) : nullptr;
+        const long long beg = static_cast<long long>(part) * d.part_len;
+        const long long end = beg + d.part_len < d.numel ? beg + d.part_len : d.numel;
+        for (long long c = beg; c < end; c += kNormPartElems) {
+            const long long sb = c + static_cast<long long>(w) * kSliceElems;  // this warp's slice
+            long long se = sb + kSliceElems;
+            if (se > end) se = end;
+            if (sb >= se) continue;
+            const bool full = se - sb == kSliceElems && (reinterpret_cast<uintptr_t>(x + sb) & 15) == 0 &&
+                              (!gr || (reinterpret_cast<uintptr_t>(gr + sb) & 7) == 0);
+            if (full) {
+                float4* xv = reinterpret_cast<float4*>(x + sb) + lane;
+                float4 r[kSliceVec];
+                if (gr) {
+                    const uint2* gv = reinterpret_cast<const uint2*>(gr + sb) + lane;
+                    uint2 gg[kSliceVec];
+#pragma unroll
+                    for (int u = 0; u < kSliceVec; ++u) {
+                        r[u] = __ldcg(xv + 32 * u);
+                        gg[u] = __ldcg(gv + 32 * u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kSliceVec; ++u) {
+                        r[u] = momentum4(r[u], gg[u], d.mu);
+                        __stcg(xv + 32 * u, r[u]);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < kSliceVec; ++u) r[u] = __ldcg(xv + 32 * u);
+                }
+#pragma unroll
+                for (int u = 0; u < kSliceVec; ++u) {
+                    s = fmaf(r[u].x, r[u].x, s);
+                    s = fmaf(r[u].y, r[u].y, s);
+                    s = fmaf(r[u].z, r[u].z, s);
+                    s = fmaf(r[u].w, r[u].w, s);
+                }
+            } else {
+                for (long long i = sb + 4LL * lane; i < se; i += 128) {
+                    for (int e = 0; e < 4; ++e) {
+                        if (i + e < se) {
+                            float v = __ldcg(x + i + e);
+                            if (gr) {
+                                v = __fadd_rn(__fmul_rn(d.mu, v), __bfloat162float(gr[i + e]));
+                                __stcg(x + i + e, v);
+                            }
+                            s = fmaf(v, v, s);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    s = warp_sum(s);
+    __syncwarp();  // every lane's stores precede lane 0's release below
+    int last = 0;
+    if (lane == 0) {
+        if (part < d.nparts) d.partial[(static_cast<long long>(g) * d.nparts + part) * kEpiWarps + w] = s;
+        if (counter) {
+            // The signal with acquire-release: the warp that completes the
+            // norm items sees every other warp's partial.
+            const int old = atom_add_acqrel_gpu(counter, 1);
+            last = old == done_target - 1;
+        }
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __syncwarp();  // lane 0's acquire precedes every lane's reads below
+    // The matrix's scale from all of its partials, in a fixed order.
+    const long long np = static_cast<long long>(d.nparts) * kEpiWarps;
+    const float* pp = d.partial + static_cast<long long>(g) * np;
+    float v = 0.0f;
+    for (long long k = lane; k < np; k += 32) v += __ldcg(pp + k);
+    v = warp_sum(v);
+    if (lane == 0) {
+        const float norm = sqrtf(v);
+        if (!isfinite(norm)) raise_error(st, kDevErrNonFinite);
+        d.scale[g] = ldexpf(1.0f, d.k_exp) / (1.05f * (norm + 1e-7f));
+        red_release_add(counter, 1);
+    }
+    __syncwarp();
+}
+
+// Cast item, one warp: once the matrix's scale is published (its counter
+// reached `wait`), this warp's slices of the part scaled and stored in fp16.
+// Returns false when the wait gave up.
+static __device__ __noinline__ bool prep_cast(const PrepDesc& d, const int* counter, int wait, const DevStatus& st,
+                                              int g, int part, int w, int lane) {
+    int ok = 1;
+    if (lane == 0 && counter) ok = wait_counter(counter, wait, st) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    __syncwarp();  // lane 0's acquire precedes every lane's reads below
+    if (part >= d.nparts) return true;
+    const float scale = __ldcg(d.scale + g);
+    const float* x = prep_f32(d.in, g);
+    __half* out = d.out + static_cast<long long>(g) * d.stride_out;
+    const int C = d.C;
+    const long long ld = d.ld_out;
+    const long long beg = static_cast<long long>(part) * d.part_len;
+    const long long end = beg + d.part_len < d.numel ? beg + d.part_len : d.numel;
+    auto h4 = [&](float4 f) {
+        __half2 h01 = __floats2half2_rn(f.x * scale, f.y * scale);
+        __half2 h23 = __floats2half2_rn(f.z * scale, f.w * scale);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&h01);
+        packed.y = *reinterpret_cast<uint32_t*>(&h23);
+        return packed;
+    };
+    for (long long c = beg; c < end; c += kNormPartElems) {
+        const long long sb = c + static_cast<long long>(w) * kSliceElems;
+        long long se = sb + kSliceElems;
+        if (se > end) se = end;
+        if (sb >= se) continue;
+        if (se - sb == kSliceElems && (reinterpret_cast<uintptr_t>(x + sb) & 15) == 0 && C % 4 == 0) {
+            const float4* xv = reinterpret_cast<const float4*>(x + sb) + lane;
+            float4 r[kSliceVec];
+#pragma unroll
+            for (int u = 0; u < kSliceVec; ++u) r[u] = __ldcg(xv + 32 * u);
+            if (ld == C) {
+                uint2* o = reinterpret_cast<uint2*>(out + sb) + lane;
+#pragma unroll
+                for (int u = 0; u < kSliceVec; ++u) o[32 * u] = h4(r[u]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < kSliceVec; ++u) {
+                    const long long i = sb + 4LL * (lane + 32 * u);
+                    const long long row = i / C;
+                    *reinterpret_cast<uint2*>(out + row * ld + (i - row * C)) = h4(r[u]);
+                }
+            }
+        } else {
+            for (long long i = sb + lane; i < se; i += 32) {
+                const long long row = i / C;
+                out[row * ld + (i - row * C)] = __float2half_rn(__ldcg(x + i) * scale);
+            }
+        }
+    }
+    return true;
 }
 
 template <int BN, int CG>
@@ -498,6 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t pub0 = smem_u32(tmem_slot + 2);  // per-buffer counts of finished epilogue warps
     CtlPhase* cph = reinterpret_cast<CtlPhase*>(tmem_slot + 4);
     CtlProb* cpb = reinterpret_cast<CtlProb*>(cph + kMaxPhases);
+    float* red = reinterpret_cast<float*>(cpb + kMaxProblems);  // kEpiWords shared words
+    int* list_len = reinterpret_cast<int*>(red + kEpiWords - 2);  // [0] all items, [1] tiles
 
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
@@ -512,11 +678,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0;  // rank in the cluster
     const uint32_t rank = crank & (CG - 1);                  // rank in the pair: 0 = leader
     const uint32_t lead = crank & ~uint32_t(CG - 1);         // cluster rank of the pair leader
-    const int unit = blockIdx.x / CL;                        // this cluster's tile walker
+    const int unit = blockIdx.x / CL;                        // this cluster's position in the walk
     const int units = gridDim.x / CL;
-    const int nwalk = P.total_tiles;
     const int nphase = P.nphase;
     const int G = P.G;
+    // This CTA's item lists: all of its cluster's items in order (epilogue),
+    // and the tiles among them (producer and MMA issuer).
+    ProgItem* ep_items = P.items + static_cast<size_t>(blockIdx.x) * 2 * P.item_cap;
+    ProgItem* mm_items = ep_items + P.item_cap;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -535,27 +704,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     for (int i = threadIdx.x; i < nphase; i += blockDim.x) {
         const GemmPhaseDesc& ph = P.phase[i];
-        cph[i] = CtlPhase{ph.tile_begin, ph.tiles_per_matrix, ph.prob_begin, ph.reverse, ph.wait_tiles};
+        cph[i] = CtlPhase{ph.item_begin, ph.tiles_per_matrix, ph.prob_begin, ph.wait};
     }
     for (int i = threadIdx.x; i < P.nprob; i += blockDim.x) {
         const GemmProblem& pr = P.prob[i];
-        cpb[i] = CtlProb{pr.tiles_per_matrix, pr.tiles_n, pr.tiles_n_walk, pr.flags, pr.K, pr.tiles_m,
+        cpb[i] = CtlProb{pr.tiles_per_matrix, pr.tiles_n, pr.flags, pr.K, pr.tiles_m,
                          pr.mA, pr.mB, pr.mAt, pr.mBt, pr.mC};
     }
     if (warp == 0 && lane == 0) {
         for (int m = 0; m < P.nmaps; ++m) prefetch_tmap(&P.maps[m]);
     }
-    // Counter value at which every tile of the phases before phase s is done.
-    auto dep_target = [&](int s) { return cph[s].wait_tiles * (kEpiWarps * CG); };
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish<CG>();
+    }
+    __syncthreads();
+    {
+        // Build this CTA's item lists: items unit, unit + units, ... of the
+        // program. Each thread decodes a contiguous range of them; a scan of
+        // the per-thread tile counts places the tiles. The lists belong to
+        // this launch alone (launches alternate between two list regions), so
+        // this overlaps the previous kernel's tail.
+        const int n_mine = P.total_items > unit ? (P.total_items - unit + units - 1) / units : 0;
+        const int per = (n_mine + kThreads - 1) / kThreads;
+        const int k0 = threadIdx.x * per < n_mine ? threadIdx.x * per : n_mine;
+        const int k1 = k0 + per < n_mine ? k0 + per : n_mine;
+        int cnt = 0;
+        for (int k = k0; k < k1; ++k) {
+            const ProgItem it = decode_item<BN, CG>(cph, cpb, nphase, G, P.prep.items, unit + k * units);
+            ep_items[k] = it;
+            cnt += item_kind(it) == kItemTile;
+        }
+        // Exclusive scan of cnt over the block's threads (warp scan, then the warp totals).
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int* wsum = reinterpret_cast<int*>(red);  // kThreads / 32 <= kEpiWords - 2 words
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int off = incl - cnt;
+        for (int w = 0; w < warp; ++w) off += wsum[w];
+        if (threadIdx.x == kThreads - 1) {
+            list_len[0] = n_mine;
+            list_len[1] = off + cnt;
+        }
+        for (int k = k0; k < k1; ++k) {
+            const ProgItem it = ep_items[k];
+            if (item_kind(it) == kItemTile) mm_items[off++] = it;
+        }
     }
     tc_fence_before();
     __syncthreads();
     if constexpr (CL > 1) cluster_sync();  // all CTAs' barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int n_items = list_len[0];
+    const int n_tiles = list_len[1];
     // Everything above overlaps the previous kernel's tail; operands written
     // by it are read only after this point.
     grid_dependency_wait();
@@ -567,10 +774,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units);
-            for (int w = unit; w < nwalk && ok; w += units) {
-                const TileInfo t = walk.decode(w);
-                const CtlProb& pr = walk.prob();
+            ProgItem nxt = n_tiles > 0 ? mm_items[0] : ProgItem{};
+            for (int k = 0; k < n_tiles && ok; ++k) {
+                const ProgItem it = nxt;
+                if (k + 1 < n_tiles) nxt = mm_items[k + 1];
+                const int g = item_matrix(it);
+                const CtlProb& pr = cpb[item_prob(it)];
                 const CUtensorMap* mapA = &P.maps[pr.mA];
                 const CUtensorMap* mapB = &P.maps[pr.mB];
                 const bool a_mn0 = pr.flags & kFlagAmn;
@@ -579,12 +788,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const bool b_sym = pr.flags & kFlagBsym;
                 const CUtensorMap* mapAt = a_sym ? &P.maps[pr.mAt] : mapA;
                 const CUtensorMap* mapBt = b_sym ? &P.maps[pr.mBt] : mapB;
-                const int ti = t.m0 / TM, tj = t.n0 / TM;
+                const int ti = it.m0 / TM, tj = it.n0 / TM;
                 const int kblocks = (pr.K + BK - 1) / BK;
-                if (P.counters && t.s > 0) {
-                    // The operands of this phase are outputs of earlier phases on
+                if (P.counters && it.wait > 0) {
+                    // The operands of this tile are outputs of earlier items on
                     // the same matrix, stored by other CTAs.
-                    if (!wait_counter(P.counters + t.g, dep_target(t.s), err)) break;
+                    if (!wait_counter(P.counters + g, it.wait, err)) break;
                     fence_proxy_async_global();
                 }
                 for (int kb = 0; kb < kblocks; ++kb) {
@@ -593,8 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         break;
                     }
                     const uint32_t fb = full0 + 8 * stage;
-                    const int arow = t.m0 + BM * static_cast<int>(rank);
-                    const int brow = t.n0 + BNH * static_cast<int>(rank);
+                    const int arow = it.m0 + BM * static_cast<int>(rank);
+                    const int brow = it.n0 + BNH * static_cast<int>(rank);
                     // Lower-only operands: a k-block right of the diagonal tile is
                     // read transposed from the tile below it.
                     const int kt = (kb * BK) / TM;
@@ -606,14 +815,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     const CUtensorMap* mB_k = b_t ? mapBt : mapB;
                     if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-                        load_operand(0, smem_u32(sA + stage * A_BYTES), mA_k, fb, a_mn, arow, BM, kb, t.g);
-                        load_operand(0, smem_u32(sB + stage * B_BYTES), mB_k, fb, b_mn, brow, BNH, kb, t.g);
+                        load_operand(0, smem_u32(sA + stage * A_BYTES), mA_k, fb, a_mn, arow, BM, kb, g);
+                        load_operand(0, smem_u32(sB + stage * B_BYTES), mB_k, fb, b_mn, brow, BNH, kb, g);
                     } else {
                         // All halves complete on the pair leader's barrier.
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (A_BYTES + B_BYTES));
                         const uint32_t lead_fb = map_to_rank(fb, lead);
-                        load_operand(1, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, t.g);
-                        load_operand(1, smem_u32(sB + stage * B_BYTES), mB_k, lead_fb, b_mn, brow, BNH, kb, t.g);
+                        load_operand(1, smem_u32(sA + stage * A_BYTES), mA_k, lead_fb, a_mn, arow, BM, kb, g);
+                        load_operand(1, smem_u32(sB + stage * B_BYTES), mB_k, lead_fb, b_mn, brow, BNH, kb, g);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -641,25 +850,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         // ------------------------------------------- MMA issuer (pair leader)
         if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0;
-            int iter = 0;
             bool ok = true;
             constexpr uint16_t kPairMask = 0x3;  // both CTAs of the pair
-            TileWalker<BN, CG> walk(cph, cpb, nphase, G, units);
             // Stage-0 descriptors of both operand layouts; a stage adds its
             // byte offset / 16 to the start-address field (addresses < 256 KB).
             const uint64_t ak0 = sw128_kmajor_desc(smem_u32(sA)), amn0 = sw128_mnmajor_desc(smem_u32(sA), kMnBlockBytes);
             const uint64_t bk0 = sw128_kmajor_desc(smem_u32(sB)), bmn0 = sw128_mnmajor_desc(smem_u32(sB), kMnBlockBytes);
-            for (int w = unit; w < nwalk && ok; w += units, ++iter) {
-                const TileInfo t = walk.decode(w);
-                const int pflags = walk.prob().flags;
-                const int kblocks = (walk.prob().K + BK - 1) / BK;
-                const int buf = iter & 1;
+            ProgItem nxt = n_tiles > 0 ? mm_items[0] : ProgItem{};
+            for (int k = 0; k < n_tiles && ok; ++k) {
+                const ProgItem it = nxt;
+                if (k + 1 < n_tiles) nxt = mm_items[k + 1];
+                const CtlProb& pr = cpb[item_prob(it)];
+                const int pflags = pr.flags;
+                const int kblocks = (pr.K + BK - 1) / BK;
+                const int buf = k & 1;
                 // First k-block read transposed (lower-only operands: the
                 // k-blocks right of the diagonal tile); MN-major operands are
                 // transposed from the first k-block on.
-                const int a_tkb = (pflags & kFlagAmn) ? 0 : (pflags & kFlagAsym) ? (t.m0 + TM) / BK : 0x7fffffff;
-                const int b_tkb = (pflags & kFlagBmn) ? 0 : (pflags & kFlagBsym) ? (t.n0 + TM) / BK : 0x7fffffff;
-                if (!mbar_wait(acce0 + 8 * buf, ((iter >> 1) & 1) ^ 1, err)) break;
+                const int a_tkb = (pflags & kFlagAmn) ? 0 : (pflags & kFlagAsym) ? (it.m0 + TM) / BK : 0x7fffffff;
+                const int b_tkb = (pflags & kFlagBmn) ? 0 : (pflags & kFlagBsym) ? (it.n0 + TM) / BK : 0x7fffffff;
+                if (!mbar_wait(acce0 + 8 * buf, ((k >> 1) & 1) ^ 1, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
                 for (int kb = 0; kb < kblocks; ++kb) {
@@ -714,19 +924,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const uint32_t acce_lead = (CG == 2) ? map_to_rank(acce0, lead) : acce0;
         uint32_t cpar = 0;  // bit k: parity of C slot k's next completion
         uint32_t cpend = 0; // bit k: a C load into slot k is in flight
-        int iter = 0;
+        int iter = 0;       // GEMM tiles done (accumulator buffer iter & 1)
         bool ok = true;
-        int ps = 0;
-        for (int w = unit; w < nwalk && ok; w += units, ++iter) {
-            const TileInfo t = decode_tile<BN, CG>(cph, cpb, nphase, G, w, ps);
-            const GemmProblem& pr = P.prob[t.p];
+        ProgItem nxt = n_items > 0 ? ep_items[0] : ProgItem{};
+        for (int k = 0; k < n_items && ok; ++k) {
+            const ProgItem it = nxt;
+            if (k + 1 < n_items) nxt = ep_items[k + 1];
+            const int kind = item_kind(it);
+            const int g = item_matrix(it);
+            if (kind != kItemTile) {
+                // Norm or cast item: each epilogue warp handles its own slice.
+                const int part = it.m0 * CG + static_cast<int>(rank);
+                int* counter = P.counters ? P.counters + g : nullptr;
+                if (kind == kItemNorm) {
+                    // The norm signals of a matrix: kEpiWarps per CTA per item.
+                    prep_norm(P.prep, counter, P.prep.items * kEpiWarps * CG, err, g, part, ew, lane);
+                } else {
+                    if (!prep_cast(P.prep, counter, it.wait, err, g, part, ew, lane)) break;
+                    // Every lane's stores precede lane 0's release.
+                    __syncwarp();
+                    if (lane == 0 && counter) red_release_add(counter, 1);
+                }
+                continue;
+            }
+            const GemmProblem& pr = P.prob[item_prob(it)];
             const int buf = iter & 1;
-            const int flags = cpb[t.p].flags;
+            const int flags = cpb[item_prob(it)].flags;
             const bool sym = flags & kFlagSym;
             const bool hasC = flags & kFlagC;
             const bool f32 = flags & kFlagOutF32;
             const int M = pr.M, N = pr.N;
-            const int r0 = t.m0 + BM * static_cast<int>(rank) + q * 32;
+            const int r0 = it.m0 + BM * static_cast<int>(rank) + q * 32;
             const int grow = r0 + lane;
             const int sr = r0 >> 5;
             // This warp's live 32 x 32 blocks of the tile, in order (bit c - cbeg).
@@ -734,33 +962,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             if (r0 < M) {
 #pragma unroll
                 for (int c = 0; c < CPW; ++c) {
-                    const int c0 = t.n0 + 32 * (cbeg + c);
+                    const int c0 = it.n0 + 32 * (cbeg + c);
                     if (c0 < N && !(sym && (c0 >> 5) > sr)) am |= 1u << c;
                 }
             }
-            const CUtensorMap* mapC = &P.maps[cpb[t.p].mC];
+            const CUtensorMap* mapC = &P.maps[cpb[item_prob(it)].mC];
             // C of block k of the list into slot k & 1 (lane 0 issues).
-            auto load_c = [&](int k, int c) {
-                const uint32_t bar = cbw + 8 * (k & 1);
+            auto load_c = [&](int kk, int c) {
+                const uint32_t bar = cbw + 8 * (kk & 1);
                 mbar_arrive_expect_tx(bar, kSlot);
-                tma_load_3d(wbase + (k & 1) * kSlot, mapC, bar, t.n0 + 32 * c, r0, t.g);
+                tma_load_3d(wbase + (kk & 1) * kSlot, mapC, bar, it.n0 + 32 * c, r0, g);
             };
             if (hasC && am) {
-                if (P.counters && t.s > 0) {
-                    // C is an earlier phase's output: acquire it like the producer.
+                if (P.counters && it.wait > 0) {
+                    // C is an earlier item's output: acquire it like the producer.
                     int okc = 1;
-                    if (lane == 0) okc = wait_counter(P.counters + t.g, dep_target(t.s), err) ? 1 : 0;
+                    if (lane == 0) okc = wait_counter(P.counters + g, it.wait, err) ? 1 : 0;
                     if (!__shfl_sync(0xffffffffu, okc, 0)) break;
                 }
                 uint32_t m = am;
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
+                for (int kk = 0; kk < 2; ++kk) {
                     if (m) {
                         if (lane == 0) {
-                            if (k == 0) fence_proxy_async_global();
-                            load_c(k, cbeg + __ffs(m) - 1);
+                            if (kk == 0) fence_proxy_async_global();
+                            load_c(kk, cbeg + __ffs(m) - 1);
                         }
-                        cpend |= 1u << k;
+                        cpend |= 1u << kk;
                         m &= m - 1;
                     }
                 }
@@ -773,23 +1001,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc_fence_after();
 
             uint32_t m = am;
-            int k = 0;
+            int kq = 0;
 #pragma unroll 1
             while (m) {
                 const int c = cbeg + __ffs(m) - 1;
                 m &= m - 1;
-                const int c0 = t.n0 + 32 * c;
-                const uint32_t slot = wbase + (k & 1) * kSlot;
+                const int c0 = it.n0 + 32 * c;
+                const uint32_t slot = wbase + (kq & 1) * kSlot;
                 uint32_t acc[32];
                 tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c * 32, acc);
                 uint4 cb[4];
                 if (hasC) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(cbw + 8 * (k & 1), (cpar >> (k & 1)) & 1, err))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(cbw + 8 * (kq & 1), (cpar >> (kq & 1)) & 1, err))) {
                         ok = false;
                         break;
                     }
-                    cpar ^= 1u << (k & 1);
-                    cpend &= ~(1u << (k & 1));
+                    cpar ^= 1u << (kq & 1);
+                    cpend &= ~(1u << (kq & 1));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) cb[kk] = ld_shared_v4(sw64_piece(slot, lane, kk));
                 }
@@ -813,23 +1041,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 // Every lane has read its C row: the slot may be overwritten.
                 __syncwarp();
                 if (flags & kFlagMuon) {
-                    muon_update_row(pr, t.g, grow, c0, v);
+                    muon_update_row(pr, g, grow, c0, v);
                 } else {
                     const bool diag_block = sym && ((c0 >> 5) == sr);
                     // Lower-only outputs mirror only inside diagonal tiles.
-                    const bool mirror = (flags & kFlagDt) && !diag_block && (!(flags & kFlagLower) || t.m0 == t.n0);
+                    const bool mirror = (flags & kFlagDt) && !diag_block && (!(flags & kFlagLower) || it.m0 == it.n0);
                     // Stage, transpose (mirror or diagonal fix-up) and store one
                     // 32 x 32 block; the slot is free again once the warp has
                     // read it back.
                     auto emit = [&](const float (&val)[32], const OutView& od, const OutView& odt) {
-                        if (f32) {
-                            emit_f32(slot, val, od, t.g, r0, c0, M, N, lane);
+                        if (P.direct_store && !mirror && !diag_block && c0 + 32 <= N && out_direct(od, f32 ? 4 : 2)) {
+                            if (grow < M) direct_row(od, g, grow, c0, val, f32);
+                        } else if (f32) {
+                            emit_f32(slot, val, od, g, r0, c0, M, N, lane);
                         } else {
                             stage_row_f16(slot, lane, val);
                             if (mirror || diag_block) stage_transpose(slot, sT, diag_block, lane);
                             __syncwarp();
-                            store_rows64<2>(slot, od, t.g, r0, c0, M, N, lane);
-                            if (mirror) store_rows64<2>(sT, odt, t.g, c0, r0, N, M, lane);
+                            store_rows64<2>(slot, od, g, r0, c0, M, N, lane);
+                            if (mirror) store_rows64<2>(sT, odt, g, c0, r0, N, M, lane);
                         }
                         __syncwarp();
                     };
@@ -843,10 +1073,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 // The C of the block two places further into the slot just freed.
                 if (hasC && m && (m & (m - 1))) {
                     const uint32_t m2 = m & (m - 1);
-                    if (lane == 0) load_c(k, cbeg + __ffs(m2) - 1);
-                    cpend |= 1u << (k & 1);
+                    if (lane == 0) load_c(kq, cbeg + __ffs(m2) - 1);
+                    cpend |= 1u << (kq & 1);
                 }
-                ++k;
+                ++kq;
             }
             if (!ok) break;
             tc_fence_before();
@@ -865,8 +1095,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     mbar_arrive(acce0 + 8 * buf);
                 else
                     mbar_arrive_cluster(acce_lead + 8 * buf);
-                if (P.counters && old % kEpiWarps == kEpiWarps - 1) red_release_add(P.counters + t.g, kEpiWarps);
+                if (P.counters && old % kEpiWarps == kEpiWarps - 1) red_release_add(P.counters + g, kEpiWarps);
             }
+            ++iter;
         }
         // C loads still in flight (only after a failed wait) land before exit.
         if (lane == 0) {
@@ -904,13 +1135,25 @@ VariantState& variant_state(int dev) {
     return st[dev];
 }
 
+// Sets the variant's dynamic shared-memory opt-in on the current device once.
+template <int BN, int CG>
+cudaError_t configure(VariantState& vs) {
+    if (!vs.configured) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemm_tc_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN, CG>());
+        if (e != cudaSuccess) return e;
+        vs.configured = true;
+    }
+    return cudaSuccess;
+}
+
 // Clusters of CG CTAs that can be resident at once with this kernel's
 // shared memory on the current device; the grid never exceeds it, so every
 // cluster of a program runs concurrently (tiles wait on tiles of other
 // clusters).
 template <int BN, int CG>
 int max_clusters(VariantState& vs, int num_sms) {
-    if (vs.clusters < 0) {
+    if (vs.clusters < 0 && configure<BN, CG>(vs) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(CG * (num_sms / CG));
         cfg.blockDim = dim3(kThreads);
@@ -929,6 +1172,10 @@ int max_clusters(VariantState& vs, int num_sms) {
         }
         vs.clusters = n;
     }
+    if (vs.clusters < 0) {
+        cudaGetLastError();
+        return num_sms / CG;
+    }
     return vs.clusters < num_sms / CG ? vs.clusters : num_sms / CG;
 }
 
@@ -940,14 +1187,13 @@ int launch_impl(const GemmProgram& prog, int num_sms, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     VariantState& vs = variant_state<BN, CG>(dev);
-    if (!vs.configured) {
-        e = cudaFuncSetAttribute(gemm_tc_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        vs.configured = true;
-    }
-    if (prog.total_tiles <= 0) return cudaSuccess;
+    e = configure<BN, CG>(vs);
+    if (e != cudaSuccess) return e;
+    if (prog.total_items <= 0) return cudaSuccess;
     const int clusters = max_clusters<BN, CG>(vs, num_sms);
-    const int grid = CG * (prog.total_tiles < clusters ? prog.total_tiles : clusters);
+    const int grid = CG * (prog.total_items < clusters ? prog.total_items : clusters);
+    // Every CTA's two lists must fit the capacity the host planned for.
+    if (static_cast<long long>(prog.item_cap) * (grid / CG) < prog.total_items) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -987,6 +1233,29 @@ int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym, int* walk_n) {
 }
 
 int gemm_signals_per_tile(int cg) { return kEpiWarps * cg; }
+
+int gemm_launch_clusters(int total_items, int bn, int cg, int num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return num_sms / cg;
+    }
+    int clusters;
+    if (cg == 2)
+        clusters = max_clusters<256, 2>(variant_state<256, 2>(dev), num_sms);
+    else if (bn == 256)
+        clusters = max_clusters<256, 1>(variant_state<256, 1>(dev), num_sms);
+    else
+        clusters = max_clusters<128, 1>(variant_state<128, 1>(dev), num_sms);
+    return total_items < clusters ? total_items : clusters;
+}
+
+size_t gemm_item_bytes(int total_items, int bn, int cg, int num_sms, int* item_cap) {
+    const int clusters = gemm_launch_clusters(total_items, bn, cg, num_sms);
+    const int cap = clusters > 0 ? (total_items + clusters - 1) / clusters : 0;
+    if (item_cap) *item_cap = cap;
+    return static_cast<size_t>(clusters) * cg * 2 * static_cast<size_t>(cap) * sizeof(ProgItem);
+}
 
 int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream) {
     if (cg == 2) return launch_impl<256, 2>(prog, num_sms, stream);

@@ -5,10 +5,12 @@
 // Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
 // easy as 1, 2, 3", SC'11): 10 rounds of two 32 x 32 -> 64-bit multiplies
 // with the published multipliers and Weyl key increments.
-// Element g of a write-back uses counter (g >> 2 low, g >> 2 high, step low,
-// step high), key (seed low, seed high), and the low 16 bits of output word
-// g & 3; the bf16 result is the high half of (bits(w) + u). NaN stays NaN
-// (made quiet), an infinity stays infinite.
+// Element g of a write-back uses counter (g >> 3 low, g >> 3 high, step low,
+// step high), key (seed low, seed high): one output (four 32-bit words)
+// serves the eight elements of a block, element g taking the 16-bit half
+// (g & 1) (low half first) of word (g & 7) >> 1. The bf16 result is the high
+// half of (bits(w) + u). NaN stays NaN (made quiet), an infinity stays
+// infinite.
 #pragma once
 
 #include <cstdint>
@@ -33,6 +35,11 @@ __device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uin
         c[2] = n2;
         c[3] = lo0;
     }
+}
+
+// The 16-bit draw of element e (0 .. 7) of a block from its Philox output.
+__device__ __forceinline__ uint32_t sr_draw(const uint32_t (&c)[4], int e) {
+    return (c[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
 }
 
 __device__ __forceinline__ uint16_t sr_bf16(float w, uint32_t u16) {

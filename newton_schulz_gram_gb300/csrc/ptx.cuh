@@ -344,6 +344,13 @@ __device__ __forceinline__ int ld_acquire(const int* addr) {
     return v;
 }
 
+// Global fetch-and-add with acquire-release semantics at GPU scope.
+__device__ __forceinline__ int atom_add_acqrel_gpu(int* addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // Shared-memory fetch-and-add with acquire-release semantics at CTA scope.
 __device__ __forceinline__ uint32_t atom_add_acqrel_cta(uint32_t smem_addr, uint32_t v) {
     uint32_t old;

@@ -27,10 +27,12 @@ What it computes:
   the element's global index", "base_index sets the global-index offset").
   The card names no generator. Reading: Philox4x32-10 (Salmon, Moraes, Dror,
   Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11). For global
-  index g = base_index + i, counter = (g >> 2 as two 32-bit words, step as two
-  32-bit words), key = (seed low word, seed high word); the element uses the
-  low 16 bits of output word g & 3. bf16 = high 16 bits of (bits(w') + u).
-  NaN stays NaN (quiet bit set); +-Inf stays as is.
+  index g = base_index + i, counter = (g >> 3 as two 32-bit words, step as two
+  32-bit words), key = (seed low word, seed high word); one output (four
+  32-bit words) serves the eight elements of a block: element g takes the
+  16-bit half (g & 1) (low half first) of output word (g & 7) >> 1.
+  bf16 = high 16 bits of (bits(w') + u). NaN stays NaN (quiet bit set);
+  +-Inf stays as is.
 """
 from __future__ import annotations
 
@@ -71,8 +73,9 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 def sr_uniform16(global_index, seed, step):
     """The 16-bit random value each element adds before truncation."""
     g = np.asarray(global_index, dtype=np.uint64)
-    blk = g >> np.uint64(2)
-    lane = (g & np.uint64(3)).astype(np.int64)
+    blk = g >> np.uint64(3)
+    lane = ((g & np.uint64(7)) >> np.uint64(1)).astype(np.int64)
+    half = (g & np.uint64(1)).astype(np.uint32)
     seed = int(seed) & 0xFFFFFFFFFFFFFFFF
     step = int(step) & 0xFFFFFFFFFFFFFFFF
     outs = philox4x32_10(blk & MASK32, blk >> np.uint64(32),
@@ -81,7 +84,7 @@ def sr_uniform16(global_index, seed, step):
                          seed & 0xFFFFFFFF, seed >> 32)
     stacked = np.stack(outs, axis=-1)
     word = np.take_along_axis(stacked, lane[..., None], axis=-1)[..., 0]
-    return (word & np.uint32(0xFFFF)).astype(np.uint32)
+    return ((word >> (np.uint32(16) * half)) & np.uint32(0xFFFF)).astype(np.uint32)
 
 
 def bf16_bits_to_f32(bits):
