@@ -622,7 +622,7 @@ BucketGeom make_geom(int R, int C) {
 // input's own orientation (R x C): Xa holds X0 (and the standard-NS iterates
 // alternate between Xa and Xb), Xb holds X after the restart.
 struct Layout {
-    size_t xa, xb, r, z, rz, qa, qb, partial, queue, counters, items, item_bytes, out32, o16, meta, total;
+    size_t xa, xb, r, z, rz, qa, qb, partial, queue, counters, sync_bytes, items, item_bytes, out32, o16, meta, total;
     long long ld_x;
     long long ld_out32;
 };
@@ -670,7 +670,8 @@ Layout make_layout(const BucketGeom& g, int Gc, int num_sms, int steps, bool nee
     L.partial = take(static_cast<size_t>(Gc) * (norm_parts(static_cast<long long>(g.R) * g.C) * kEpiWarps + 1) * 4);
     // The norm/cast queue (1 + Gc ints) and the GEMM counters (Gc ints),
     // adjacent so that one clear covers both.
-    L.queue = take((1 + 2 * static_cast<size_t>(Gc)) * 4);
+    L.sync_bytes = (1 + 2 * static_cast<size_t>(Gc)) * 4;
+    L.queue = take(L.sync_bytes);
     L.counters = L.queue + (1 + static_cast<size_t>(Gc)) * 4;
     L.item_bytes = item_region_bytes(g, Gc, num_sms, steps);
     L.items = take(L.item_bytes);
@@ -708,8 +709,9 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     // Stored copies of X in the input's orientation (R x C).
     Mat Xa = mat16(ws, L.xa, g.R, g.C, L.ld_x);
     Mat Xb = mat16(ws, L.xb, g.R, g.C, L.ld_x);
-    // The norm/cast queue and the GEMM counters start at zero.
-    CK(cudaMemsetAsync(ws + L.queue, 0, (1 + 2 * static_cast<size_t>(Gc)) * sizeof(int), s));
+    // The norm/cast queue and the GEMM counters start at zero (the whole
+    // region: a last, smaller chunk still uses the layout's offsets).
+    CK(cudaMemsetAsync(ws + L.queue, 0, L.sync_bytes, s));
     prog.counters_cleared();
     if (!prep_in_program()) {
         // Norm, scale and fp16 cast (with the momentum update first, for the

@@ -44,7 +44,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 static_assert(sizeof(GemmProgram) <= 32764, "kernel parameter block too large");
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
+constexpr int kDepWarp = 2 + kEpiWarps;       // the dependency warp follows the epilogue warps
+constexpr int kThreads = 32 * (kDepWarp + 1);  // producer, MMA, epilogue, dependency
+constexpr int kDepRing = 4;                    // tiles the dependency warp may run ahead
 
 // Per-warp epilogue shared memory: three 2 KB slots of 32 rows x 64 bytes
 // (64-byte swizzle). Slots 0 and 1 receive, by TMA, the C addend of the
@@ -88,7 +90,7 @@ constexpr int kCtlBytes = kMaxPhases * static_cast<int>(sizeof(CtlPhase)) + kMax
 // Shared words of the epilogue group: the per-warp values of a reduction,
 // a broadcast flag and the list lengths.
 constexpr int kEpiWords = 16;
-__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 5 + 2 * kEpiWarps; }
+__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 5 + 2 * kEpiWarps + 2 * kDepRing; }
 
 template <int BN, int CG>
 constexpr int smem_bytes() {
@@ -671,6 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t acce0 = smem_u32(bars + 2 * STAGES + 2);
     const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
     const uint32_t cbar0 = smem_u32(bars + 2 * STAGES + 5);  // two C-slot barriers per epilogue warp
+    // Dependency ring: slot j's "ready" and "free" barriers.
+    const uint32_t depf0 = smem_u32(bars + 2 * STAGES + 5 + 2 * kEpiWarps);
+    const uint32_t depe0 = depf0 + 8 * kDepRing;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -698,6 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         mbar_init(drain_bar, 1);
         for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(cbar0 + 8 * b, 1);
+        for (int b = 0; b < kDepRing; ++b) {
+            mbar_init(depf0 + 8 * b, 1);
+            mbar_init(depe0 + 8 * b, 1);
+        }
         tmem_slot[2] = 0;
         tmem_slot[3] = 0;
         fence_mbar_init();
@@ -790,11 +799,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const CUtensorMap* mapBt = b_sym ? &P.maps[pr.mBt] : mapB;
                 const int ti = it.m0 / TM, tj = it.n0 / TM;
                 const int kblocks = (pr.K + BK - 1) / BK;
-                if (P.counters && it.wait > 0) {
+                {
                     // The operands of this tile are outputs of earlier items on
-                    // the same matrix, stored by other CTAs.
-                    if (!wait_counter(P.counters + g, it.wait, err)) break;
-                    fence_proxy_async_global();
+                    // the same matrix, stored by other CTAs: the dependency
+                    // warp has acquired them (its release on the ring slot
+                    // orders that acquire before these loads).
+                    const int slot = k % kDepRing;
+                    if (!mbar_wait(depf0 + 8 * slot, (k / kDepRing) & 1, err)) break;
+                    mbar_arrive(depe0 + 8 * slot);
+                    if (it.wait > 0) fence_proxy_async_global();
                 }
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, err)) {
@@ -910,6 +923,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // All MMAs issued by this thread must finish before TMEM is freed.
             tc_commit<CG>(drain_bar);
             drain_wait(drain_bar, 0, err.limit_ns);
+        }
+        __syncwarp();
+    } else if (warp == kDepWarp) {
+        // ----------------------------------------------------- dependencies
+        // Acquires each tile's dependency (the counter of its matrix) up to
+        // kDepRing tiles ahead of the producer, so that the producer's loads
+        // never wait for an acquire's round trip to memory.
+        if (lane == 0) {
+            for (int k = 0; k < n_tiles; ++k) {
+                const int slot = k % kDepRing;
+                if (!mbar_wait(depe0 + 8 * slot, ((k / kDepRing) & 1) ^ 1, err)) break;
+                const ProgItem it = mm_items[k];
+                if (P.counters && it.wait > 0 && !wait_counter(P.counters + item_matrix(it), it.wait, err)) break;
+                mbar_arrive(depf0 + 8 * slot);
+            }
         }
         __syncwarp();
     } else {
