@@ -317,6 +317,11 @@ bool prep_in_program() {
     return e && std::string(e) == "program";
 }
 
+bool self_sym() {
+    const char* e = std::getenv("GNS_SELF_SYM");
+    return !(e && std::atoi(e) == 0);
+}
+
 // Full-width output blocks are stored straight from registers unless
 // GNS_DIRECT_STORE=0 (staged through shared memory).
 bool direct_store() {
@@ -497,6 +502,12 @@ class ProgramBuilder {
         if (sp.lower) flags |= kFlagLower;
         if (sp.muon) flags |= kFlagMuon;
         if (!sp.sym && col_walk()) flags |= kFlagColWalk;
+        // A symmetric product of one stored matrix with itself (X X^T, R R,
+        // A A): with an exactly symmetric addend, its diagonal tiles are
+        // exactly symmetric as computed (GNS_SELF_SYM=0 mirrors them instead).
+        if (sp.sym && sp.A.p == sp.B.p && sp.A.ld == sp.B.ld && sp.A.stride == sp.B.stride && sp.A.rows == sp.B.rows &&
+            sp.A.cols == sp.B.cols && sp.a_mn == sp.b_mn && sp.a_sym == sp.b_sym && self_sym())
+            flags |= kFlagSelfSym;
         if (sp.C) {
             flags |= kFlagC;
             pr.C = static_cast<const __half*>(sp.C->p);

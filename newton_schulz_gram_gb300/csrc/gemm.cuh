@@ -60,7 +60,14 @@ enum GemmFlags : int {
     // Non-symmetric product walked column by column: the tiles sharing a B
     // column block run together, so B (for Q X, the large X) is read from
     // DRAM about once and hits L2 for the other tile rows.
-    kFlagColWalk = 4096
+    kFlagColWalk = 4096,
+    // Symmetric product of one matrix with itself (A and B the same stored
+    // operand, and C exactly symmetric): every element (i, j) and (j, i) is
+    // the same sum of the same products in the same order, so the
+    // accumulator of a diagonal tile is exactly symmetric and all of its
+    // blocks, above the diagonal too, are written as computed, with no
+    // mirrored copy (square tiles only).
+    kFlagSelfSym = 8192
 };
 
 // Parameters of the fused Muon update (kFlagMuon).

@@ -985,13 +985,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const int r0 = it.m0 + BM * static_cast<int>(rank) + q * 32;
             const int grow = r0 + lane;
             const int sr = r0 >> 5;
+            // A diagonal tile of a product of a matrix with itself: written
+            // whole as computed (no upper blocks skipped, nothing mirrored).
+            const bool whole = (flags & kFlagSelfSym) && TM == BN && it.m0 == it.n0;
             // This warp's live 32 x 32 blocks of the tile, in order (bit c - cbeg).
             uint32_t am = 0;
             if (r0 < M) {
 #pragma unroll
                 for (int c = 0; c < CPW; ++c) {
                     const int c0 = it.n0 + 32 * (cbeg + c);
-                    if (c0 < N && !(sym && (c0 >> 5) > sr)) am |= 1u << c;
+                    if (c0 < N && !(sym && !whole && (c0 >> 5) > sr)) am |= 1u << c;
                 }
             }
             const CUtensorMap* mapC = &P.maps[cpb[item_prob(it)].mC];
@@ -1071,9 +1074,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 if (flags & kFlagMuon) {
                     muon_update_row(pr, g, grow, c0, v);
                 } else {
-                    const bool diag_block = sym && ((c0 >> 5) == sr);
+                    const bool diag_block = sym && !whole && ((c0 >> 5) == sr);
                     // Lower-only outputs mirror only inside diagonal tiles.
-                    const bool mirror = (flags & kFlagDt) && !diag_block && (!(flags & kFlagLower) || it.m0 == it.n0);
+                    const bool mirror = (flags & kFlagDt) && !diag_block && !whole &&
+                                        (!(flags & kFlagLower) || it.m0 == it.n0);
                     // Stage, transpose (mirror or diagonal fix-up) and store one
                     // 32 x 32 block; the slot is free again once the warp has
                     // read it back.
