@@ -367,16 +367,7 @@ def llama7b_line(gns, torch, stream, dev, peaks):
     nc_gbs = 12.0 * params / (nc_step_ms / 1e3) / 1e9 if nc_ms > 0 else None
     del W, Gr, M
     torch.cuda.empty_cache()
-    # The standalone update kernel (W <- SR_bf16(decay W - step O)) over 2^30
-    # elements: W read and written, O read, 6 B per element.
-    N = 1 << 30
-    w = torch.zeros(N, dtype=torch.bfloat16, device=dev).view(32768, 32768)
-    o = torch.zeros(N, dtype=torch.float16, device=dev).view(32768, 32768)
-    ums, uq = time_calls(torch, stream, lambda: gns.gns_muon_update(w, o, 0.02, 0.01, 1.0, 0, 1), calls=1,
-                         warmup=2, blocks=10)
-    del w, o
-    torch.cuda.empty_cache()
-    upd_gbs = 6.0 * N / (ums / 1e3) / 1e9
+    upd = update_rate(gns, torch, stream, dev, 30, peaks)
     return {"workload": "llama7b_muon_step (224 matrices, 6.98e9 params, buckets by shape)",
             "ms_per_step": ms, "ms_quartiles": q, "params": params, "algorithmic_tflops": alg / (ms / 1e3) / 1e12,
             "frac_of_peak": alg / (ms / 1e3) / 1e12 / peaks["tflops_sustained"],
@@ -384,8 +375,26 @@ def llama7b_line(gns, torch, stream, dev, peaks):
             "elementwise": {
                 "norm_cast_momentum": {"ms_per_step": nc_step_ms, "launches_per_step": nc_n / 3, "gbs": nc_gbs,
                                        "bytes_per_element": 12, "frac_of_hbm": (nc_gbs / peaks["hbm_gbs"]) if nc_gbs else None},
-                "muon_update_kernel": {"elements": N, "ms": ums, "ms_quartiles": uq, "gbs": upd_gbs,
-                                       "bytes_per_element": 6, "frac_of_hbm": upd_gbs / peaks["hbm_gbs"]}}}
+                "muon_update_kernel": upd}}
+
+
+def update_rate(gns, torch, stream, dev, log2n, peaks, blocks=10):
+    """The standalone update kernel (W <- SR_bf16(decay W - step O)) over
+    2^log2n elements of a square matrix: W read and written, O read, 6 B per
+    element; O ~ N(0, 1) in fp16 so every element takes the rounding path."""
+    N = 1 << log2n
+    side = 1 << (log2n // 2)
+    w = (0.02 * torch.randn(side, N // side, device=dev)).to(torch.bfloat16)
+    o = torch.randn(side, N // side, device=dev).to(torch.float16)
+    ums, uq = time_calls(torch, stream, lambda: gns.gns_muon_update(w, o, 0.02, 0.01, 1.0, 0, 1), calls=1,
+                         warmup=2, blocks=blocks)
+    if gns.gns_get_status() != 0:
+        raise SystemExit("device status error in the update kernel")
+    del w, o
+    torch.cuda.empty_cache()
+    gbs = 6.0 * N / (ums / 1e3) / 1e9
+    return {"elements": N, "ms": ums, "ms_quartiles": uq, "gbs": gbs, "bytes_per_element": 6,
+            "frac_of_hbm": gbs / peaks["hbm_gbs"]}
 
 
 def single_thread_oracle(budget_s=10.0):
@@ -425,9 +434,20 @@ def main():
     ap.add_argument("--record-traffic", metavar="CSV",
                     help="write the GEMM traffic summary from an ncu --csv --page raw capture and exit")
     ap.add_argument("--traffic-matrices", type=int, default=12, help="matrices in the captured launch")
+    ap.add_argument("--only-update", type=int, metavar="LOG2N",
+                    help="time only the standalone Muon update kernel on 2^LOG2N elements, print its rate and exit")
     args = ap.parse_args()
     if args.record_traffic:
         return record_traffic(args.record_traffic, args.traffic_matrices)
+    if args.only_update:
+        import torch
+        import newton_schulz_gram_gb300 as gns
+        gns.load()
+        dev = torch.device("cuda", 0)
+        r = update_rate(gns, torch, torch.cuda.current_stream(dev), dev, args.only_update, load_peaks(),
+                        blocks=max(3, args.steps // 4))
+        print(json.dumps({"kernel": "muon_update_kernel", **r}))
+        return
     global G
     G = args.G
     if args.warmup < 3:

@@ -75,7 +75,6 @@ struct DeviceState {
     int* err = nullptr;      // status block: [0] status word, [1] abort mark (see DevStatus)
     int epoch = 0;           // number of the current call on this device
     DevStatus status{};      // the current call's device-side error reporting
-    unsigned gemm_launches = 0;  // GEMM launches so far: selects the work-list half
     float* stage = nullptr;  // device staging for the host-buffer entry point
     size_t stage_bytes = 0;
     cudaStream_t h2d = nullptr, d2h = nullptr;  // copy streams of the host-buffer entry point
@@ -159,7 +158,6 @@ struct NoAllocDevice {
     int num_sms = 0;
     int cc_major = 0, cc_minor = 0;
     int epoch = 0;            // number of the current allocation-free call on this device
-    unsigned gemm_launches = 0;  // its GEMM launches so far (selects the work-list half)
 };
 
 std::mutex g_noalloc_mu;
@@ -310,13 +308,6 @@ TileShape choose_tile(int n, int G, int num_sms) {
     return {256, 2};
 }
 
-// The norm and fp16 cast run as a kernel of their own before the GEMM
-// program, or with GNS_PREP=program as the program's first items.
-bool prep_in_program() {
-    const char* e = std::getenv("GNS_PREP");
-    return e && std::string(e) == "program";
-}
-
 bool self_sym() {
     const char* e = std::getenv("GNS_SELF_SYM");
     return !(e && std::atoi(e) == 0);
@@ -327,6 +318,16 @@ bool self_sym() {
 bool direct_store() {
     const char* e = std::getenv("GNS_DIRECT_STORE");
     return !(e && std::atoi(e) == 0);
+}
+
+// How many tiles ahead of its producer a CTA pair claims (GNS_LOOKAHEAD,
+// 1 .. 8; default 1): enough to hide the claim, the decode and the
+// dependency acquire, few enough that no CTA holds tiles another CTA could
+// start sooner.
+int lookahead() {
+    const char* e = std::getenv("GNS_LOOKAHEAD");
+    const int v = e ? std::atoi(e) : 1;
+    return v < 1 ? 1 : (v > 8 ? 8 : v);
 }
 
 // Non-symmetric products walk their tiles column by column unless
@@ -340,22 +341,16 @@ bool col_walk() {
 // problems that read or write the same buffer with the same box.
 //
 // The launch's work list (see gemm.cuh) is numbered here: each phase gets
-// its first list index and the counter target of its tiles (the signals of
-// every earlier item of the same matrix). The kernel builds each CTA's part
-// of the list in `items`, a region of two halves that consecutive launches
-// alternate between, so a launch's list building never overwrites the list
-// of the launch before it while that one finishes.
+// its first ticket and the counter target of its tiles (the signals of
+// every earlier tile of the same matrix).
 class ProgramBuilder {
   public:
-    ProgramBuilder(DeviceState& st, int G, TileShape ts, int* counters, char* items, size_t item_bytes,
-                   cudaStream_t s)
-        : st_(st), G_(G), ts_(ts), counters_(counters), items_(items), item_half_(item_bytes / 2), s_(s) {
+    // sync: 1 + G ints in device memory, the launch's ticket counter
+    // followed by the per-matrix counters.
+    ProgramBuilder(DeviceState& st, int G, TileShape ts, int* sync, cudaStream_t s)
+        : st_(st), G_(G), ts_(ts), sync_(sync), s_(s) {
         reset();
     }
-
-    // The first launch starts with the norm and cast of the bucket's fp32
-    // matrices (prep items), interleaved with its first phase.
-    void set_prep(const PrepDesc& d) { prep_ = d; }
 
     // Adds a phase of one or two independent problems; launches first when
     // the program is full (the next launch then depends on it by stream order).
@@ -376,12 +371,6 @@ class ProgramBuilder {
             prog_.nprob += 1;
         }
         const long long spi = gemm_signals_per_tile(ts_.cg);
-        if (prog_.nphase == 0 && prep_.items > 0) {
-            // The prep items come first: per matrix q norm and q cast items
-            // and the scale's signal.
-            items_done_ = 2LL * prep_.items * G_;
-            signals_done_ = 2LL * prep_.items * spi + 1;
-        }
         const long long per = ph.tiles_per_matrix;
         if (items_done_ + per * G_ > (1LL << 30) || signals_done_ + per * spi > (1LL << 30))
             return fail(GNS_ERR_INVALID, "program too large for one launch");
@@ -399,27 +388,17 @@ class ProgramBuilder {
 
     int flush() {
         if (prog_.nphase == 0) return GNS_OK;
-        if (prog_.nphase > 1 || prep_.items > 0) {
-            if (!counters_) return fail(GNS_ERR_INVALID, "a multi-phase program needs counters");
-            prog_.counters = counters_;
-            if (!cleared_) CK(cudaMemsetAsync(counters_, 0, sizeof(int) * static_cast<size_t>(G_), s_));
-        } else {
-            prog_.counters = nullptr;
-        }
-        prog_.prep = prep_;
+        // The ticket counter and the matrices' counters start at zero.
+        if (!cleared_) CK(cudaMemsetAsync(sync_, 0, sizeof(int) * (1 + static_cast<size_t>(G_)), s_));
+        prog_.ticket = sync_;
+        prog_.counters = prog_.nphase > 1 ? sync_ + 1 : nullptr;
         prog_.direct_store = direct_store() ? 1 : 0;
+        prog_.lookahead = lookahead();
         prog_.st = st_.status;
         prog_.G = G_;
-        int cap = 0;
-        const size_t need = gemm_item_bytes(prog_.total_items, ts_.bn, ts_.cg, st_.num_sms, &cap);
-        if (need > item_half_) return fail(GNS_ERR_INVALID, "the work list region is too small");
-        prog_.items = reinterpret_cast<ProgItem*>(items_ + ((st_.gemm_launches & 1) ? item_half_ : 0));
-        prog_.item_cap = cap;
-        st_.gemm_launches += 1;
         cudaStream_t s = s_;
         LAUNCH(kClsGemm, launch_gemm_program(prog_, ts_.bn, ts_.cg, st_.num_sms, s));
         reset();
-        prep_.items = 0;  // only the first launch of a call starts from the fp32 input
         cleared_ = false;
         return GNS_OK;
     }
@@ -543,12 +522,9 @@ class ProgramBuilder {
     DeviceState& st_;
     int G_;
     TileShape ts_;
-    int* counters_;
-    char* items_;
-    size_t item_half_;
+    int* sync_;
     cudaStream_t s_;
     GemmProgram prog_;
-    PrepDesc prep_{};
     bool cleared_ = false;
     std::vector<std::string> keys_;
     long long items_done_ = 0;    // list items of the phases added so far
@@ -633,33 +609,12 @@ BucketGeom make_geom(int R, int C) {
 // input's own orientation (R x C): Xa holds X0 (and the standard-NS iterates
 // alternate between Xa and Xb), Xb holds X after the restart.
 struct Layout {
-    size_t xa, xb, r, z, rz, qa, qb, partial, queue, counters, sync_bytes, items, item_bytes, out32, o16, meta, total;
+    size_t xa, xb, r, z, rz, qa, qb, partial, queue, sync, sync_bytes, out32, o16, meta, total;
     long long ld_x;
     long long ld_out32;
 };
 
-// Bytes of the GEMM program's work-list region (both halves) for a chunk of
-// Gc matrices: an upper bound on the items of any launch of the chunk (the
-// prep items, at most 5 steps + 1 symmetric products and steps + 1 Q X
-// products per matrix, counted with the smallest tiles the planner picks).
-size_t item_region_bytes(const BucketGeom& g, int Gc, int num_sms, int steps) {
-    long long worst = 0;
-    for (const TileShape ts : {TileShape{128, 1}, TileShape{256, 1}, TileShape{256, 2}}) {
-        const long long sym = gemm_tiles_per_matrix(g.n, g.n, ts.bn, ts.cg, true, nullptr);
-        const long long gen = gemm_tiles_per_matrix(g.R, g.C, ts.bn, ts.cg, false, nullptr);
-        const long long prep = 2LL * ((norm_parts(static_cast<long long>(g.R) * g.C) + ts.cg - 1) / ts.cg);
-        const long long per = prep + (5LL * steps + 1) * sym + (steps + 1LL) * gen;
-        const long long total = std::min<long long>(per * Gc, 1LL << 30);
-        worst = std::max(worst, total);
-    }
-    size_t worst_bytes = 0;
-    for (const TileShape ts : {TileShape{128, 1}, TileShape{256, 1}, TileShape{256, 2}})
-        worst_bytes = std::max(worst_bytes, gemm_item_bytes(static_cast<int>(worst), ts.bn, ts.cg, num_sms, nullptr));
-    return 2 * worst_bytes;
-}
-
-Layout make_layout(const BucketGeom& g, int Gc, int num_sms, int steps, bool need_out32, bool need_o16,
-                   size_t meta_bytes) {
+Layout make_layout(const BucketGeom& g, int Gc, bool need_out32, bool need_o16, size_t meta_bytes) {
     Layout L{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -677,15 +632,13 @@ Layout make_layout(const BucketGeom& g, int Gc, int num_sms, int steps, bool nee
     L.rz = g.square ? 0 : take(nn);
     L.qa = g.square ? 0 : take(nn);
     L.qb = g.square ? 0 : take(nn);
-    // Norm partials (one per epilogue warp and part), then the scales.
-    L.partial = take(static_cast<size_t>(Gc) * (norm_parts(static_cast<long long>(g.R) * g.C) * kEpiWarps + 1) * 4);
-    // The norm/cast queue (1 + Gc ints) and the GEMM counters (Gc ints),
-    // adjacent so that one clear covers both.
-    L.sync_bytes = (1 + 2 * static_cast<size_t>(Gc)) * 4;
+    L.partial = take(static_cast<size_t>(Gc) * norm_parts(static_cast<long long>(g.R) * g.C) * 4);
+    // The norm/cast queue (1 + Gc ints), then the GEMM program's ticket and
+    // per-matrix counters (1 + Gc ints): adjacent, so that one clear covers
+    // both.
+    L.sync_bytes = (2 + 2 * static_cast<size_t>(Gc)) * 4;
     L.queue = take(L.sync_bytes);
-    L.counters = L.queue + (1 + static_cast<size_t>(Gc)) * 4;
-    L.item_bytes = item_region_bytes(g, Gc, num_sms, steps);
-    L.items = take(L.item_bytes);
+    L.sync = L.queue + (1 + static_cast<size_t>(Gc)) * 4;
     L.ld_out32 = round_up_ll(g.C, 4);
     L.out32 = need_out32 ? take(static_cast<size_t>(g.R) * L.ld_out32 * 4 * Gc) : 0;
     L.o16 = need_o16 ? take(static_cast<size_t>(g.R) * round_up_ll(g.C, 8) * 2 * Gc) : 0;
@@ -712,7 +665,7 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
              cudaStream_t s) {
     const TileShape ts = choose_tile(g.n, Gc, st.num_sms);
     char* ws = st.ws;
-    ProgramBuilder prog(st, Gc, ts, reinterpret_cast<int*>(ws + L.counters), ws + L.items, L.item_bytes, s);
+    ProgramBuilder prog(st, Gc, ts, reinterpret_cast<int*>(ws + L.sync), s);
     // Symmetric n x n intermediates are stored lower-only (diagonal tiles in
     // full) when the tiles are square.
     const bool lo = ts.bn == 128 * ts.cg;
@@ -724,9 +677,9 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
     // region: a last, smaller chunk still uses the layout's offsets).
     CK(cudaMemsetAsync(ws + L.queue, 0, L.sync_bytes, s));
     prog.counters_cleared();
-    if (!prep_in_program()) {
+    {
         // Norm, scale and fp16 cast (with the momentum update first, for the
-        // Muon step) as a kernel of its own before the GEMM program.
+        // Muon step), right before the GEMM program.
         NormCastJob job{};
         job.in = in;
         if (grads) job.grads = *grads;
@@ -742,28 +695,6 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
         job.queue = reinterpret_cast<int*>(ws + L.queue);
         job.st = st.status;
         LAUNCH(kClsNorm, launch_norm_cast(job, st.num_sms, s));
-    } else {
-        // The same as the first items of the GEMM program.
-        PrepDesc pd{};
-        pd.in = in;
-        if (grads) {
-            pd.grads = *grads;
-            pd.momentum = 1;
-        }
-        pd.mu = mu;
-        pd.R = g.R;
-        pd.C = g.C;
-        pd.k_exp = g.k_exp;
-        pd.numel = static_cast<long long>(g.R) * g.C;
-        pd.nparts = norm_parts(pd.numel);
-        pd.part_len = norm_part_len(pd.numel);
-        pd.out = static_cast<__half*>(Xa.p);
-        pd.ld_out = Xa.ld;
-        pd.stride_out = Xa.stride;
-        pd.partial = reinterpret_cast<float*>(ws + L.partial);
-        pd.scale = pd.partial + static_cast<size_t>(Gc) * pd.nparts * kEpiWarps;
-        pd.items = (pd.nparts + ts.cg - 1) / ts.cg;
-        prog.set_prep(pd);
     }
     const float inv_s = 1.0f / g.s;
     const float out_scale = std::ldexp(1.0f, -g.k_exp);
@@ -962,8 +893,8 @@ int validate_common(int G, int R, int C, int steps) {
     return GNS_OK;
 }
 
-int chunk_size(const BucketGeom& g, int G, int num_sms, int steps, bool out32, bool o16) {
-    const Layout one = make_layout(g, 1, num_sms, steps, out32, o16, 0);
+int chunk_size(const BucketGeom& g, int G, bool out32, bool o16) {
+    const Layout one = make_layout(g, 1, out32, o16, 0);
     size_t per = one.total;
     size_t cap = chunk_cap_bytes();
     long long c = static_cast<long long>(cap / std::max<size_t>(per, 1));
@@ -985,8 +916,8 @@ int orthogonalize_device(float* ptr, int G, int R, int C, int steps, uint64_t re
     RET(load_coeffs(coeffs, steps, cf));
     const BucketGeom g = make_geom(R, C);
     const bool direct_out = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && ((static_cast<long long>(C) * 4) % 16 == 0);
-    const int Gc = chunk_size(g, G, st->num_sms, steps, !direct_out, false);
-    const Layout L = make_layout(g, Gc, st->num_sms, steps, !direct_out, false, 0);
+    const int Gc = chunk_size(g, G, !direct_out, false);
+    const Layout L = make_layout(g, Gc, !direct_out, false, 0);
     RET(ensure_workspace(*st, L.total));
     const long long numel = static_cast<long long>(R) * C;
     for (int g0 = 0; g0 < G; g0 += Gc) {
@@ -1067,14 +998,13 @@ int optimizer_step(const gns_tensor* params, const gns_tensor* grads, const gns_
         // NorMuon needs all of O before its row statistics: it stores O.
         const bool fused = !vm && muon_fused();
         const size_t per_matrix_meta = narr * sizeof(void*) + sizeof(long long) + (vm ? 4 * sizeof(float) * R : 0);
-        int Gc = chunk_size(g, G, st->num_sms, 5, false, !fused);
+        int Gc = chunk_size(g, G, false, !fused);
         // The statistics buffers live in the metadata block.
-        while (Gc > 1 && make_layout(g, Gc, st->num_sms, 5, false, !fused,
-                                     static_cast<size_t>(Gc) * per_matrix_meta + 1024).total >
+        while (Gc > 1 && make_layout(g, Gc, false, !fused, static_cast<size_t>(Gc) * per_matrix_meta + 1024).total >
                              chunk_cap_bytes())
             --Gc;
         const size_t meta_bytes = static_cast<size_t>(Gc) * per_matrix_meta + 1024;
-        const Layout L = make_layout(g, Gc, st->num_sms, 5, false, !fused, meta_bytes);
+        const Layout L = make_layout(g, Gc, false, !fused, meta_bytes);
         RET(ensure_workspace(*st, L.total));
         const long long ld_o = round_up_ll(C, 8);
         const float scale = 0.2f * std::sqrt(static_cast<float>(std::max(R, C)));
@@ -1137,7 +1067,8 @@ int optimizer_step(const gns_tensor* params, const gns_tensor* grads, const gns_
                 LAUNCH(kClsMuon, launch_normuon_factor(row_sq, row_hat, inv, gc, R, lr * scale, steps, s));
                 row_step = steps;
             }
-            LAUNCH(kClsMuon, launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step, s,
+            LAUNCH(kClsMuon, launch_muon_update(Ws, Os, ld_o, bases_dev, 0, gc, R, C, lr, wd, scale, seed, step,
+                                                st->num_sms, s,
                                                 row_step));
         }
     }
@@ -1194,9 +1125,9 @@ int dion3_step_impl(const gns_tensor* params, const gns_tensor* grads, const gns
                                 4 * static_cast<size_t>(k) + 4 * static_cast<size_t>(k) * m + 1024;
         int Gc = std::min(G, 65535);
         while (Gc > 1 &&
-               make_layout(g, Gc, st->num_sms, 5, false, true, static_cast<size_t>(Gc) * per_meta).total > chunk_cap_bytes())
+               make_layout(g, Gc, false, true, static_cast<size_t>(Gc) * per_meta).total > chunk_cap_bytes())
             Gc = (Gc + 1) / 2;
-        const Layout L = make_layout(g, Gc, st->num_sms, 5, false, true, static_cast<size_t>(Gc) * per_meta);
+        const Layout L = make_layout(g, Gc, false, true, static_cast<size_t>(Gc) * per_meta);
         RET(ensure_workspace(*st, L.total));
         const long long ld_o = round_up_ll(m, 8);
         for (int g0 = 0; g0 < G; g0 += Gc) {
@@ -1415,7 +1346,8 @@ int gns_muon_update(uint16_t* W_bf16, const uint16_t* O_fp16, int rows, int cols
     MatrixSet Ws{W_bf16, numel, nullptr};
     MatrixSet Os{O_fp16, numel, nullptr};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    LAUNCH(kClsMuon, launch_muon_update(Ws, Os, cols, nullptr, base_index, 1, rows, cols, lr, wd, scale, seed, step, s));
+    LAUNCH(kClsMuon, launch_muon_update(Ws, Os, cols, nullptr, base_index, 1, rows, cols, lr, wd, scale, seed, step,
+                                        st->num_sms, s));
     return GNS_OK;
 }
 
@@ -1445,10 +1377,8 @@ int gns_symm_gemm(const void* A, const void* B, const void* C, void* D, int G, i
     p.sym = true;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const TileShape ts = choose_tile(n, G, st->num_sms);
-    const size_t item_bytes =
-        2 * gemm_item_bytes(G * gemm_tiles_per_matrix(n, n, ts.bn, ts.cg, true, nullptr), ts.bn, ts.cg, st->num_sms, nullptr);
-    RET(ensure_workspace(*st, item_bytes));
-    ProgramBuilder prog(*st, G, ts, nullptr, st->ws, item_bytes, s);
+    RET(ensure_workspace(*st, 256));
+    ProgramBuilder prog(*st, G, ts, reinterpret_cast<int*>(st->ws), s);
     RET(prog.phase(p, nullptr));
     return prog.flush();
 }
@@ -1631,14 +1561,14 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
     const bool direct_out = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && ((static_cast<long long>(C) * 4) % 16 == 0);
     // Largest chunk of matrices whose workspace fits in the fixed array.
     const size_t avail = kNoAllocBytes - kNoAllocStatusBytes;
-    const size_t per = make_layout(g, 1, nd.num_sms, steps, !direct_out, false, 0).total;
+    const size_t per = make_layout(g, 1, !direct_out, false, 0).total;
     if (per > avail)
         return fail(GNS_ERR_INVALID, "a " + std::to_string(R) + " x " + std::to_string(C) + " matrix needs " +
                                          std::to_string(per) + " bytes of workspace; the allocation-free entry point has " +
                                          std::to_string(avail) + " bytes");
     int Gc = static_cast<int>(std::min<size_t>(std::min<size_t>(G, 65535), avail / per));
-    while (Gc > 1 && make_layout(g, Gc, nd.num_sms, steps, !direct_out, false, 0).total > avail) --Gc;
-    const Layout L = make_layout(g, Gc, nd.num_sms, steps, !direct_out, false, 0);
+    while (Gc > 1 && make_layout(g, Gc, !direct_out, false, 0).total > avail) --Gc;
+    const Layout L = make_layout(g, Gc, !direct_out, false, 0);
 
     DeviceState st;
     st.device = dev;
@@ -1647,7 +1577,6 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
     st.cc_minor = nd.cc_minor;
     st.err = reinterpret_cast<int*>(nd.scratch);
     st.epoch = nd.epoch;
-    st.gemm_launches = nd.gemm_launches;
     st.status = DevStatus{st.err, st.epoch, 0, wait_limit_ns()};
     st.ws = nd.scratch + kNoAllocStatusBytes;
     st.ws_bytes = avail;
@@ -1676,12 +1605,7 @@ extern "C" int gns_orthogonalize_batched_noalloc(float* ptr, int G, int R, int C
             os.out.ld = L.ld_out32;
             os.out.stride = static_cast<long long>(R) * L.ld_out32;
         }
-        const int rc = run_core(st, g, L, gc, in, nullptr, 0.0f, steps, periodic_restarts(steps, restart_at), cf, os, s);
-        {
-            std::lock_guard<std::mutex> lk(g_noalloc_mu);
-            g_noalloc[dev].gemm_launches = st.gemm_launches;
-        }
-        RET(rc);
+        RET(run_core(st, g, L, gc, in, nullptr, 0.0f, steps, periodic_restarts(steps, restart_at), cf, os, s));
         if (!direct_out)
             LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, base, gc, R, C, s));
     }

@@ -472,19 +472,30 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
     const long long nblk = blk_last - blk_first + 1;
     const bool fast = ((base & 7) == 0) && (C % 8 == 0) && (ld_o % 8 == 0) &&
                       ((reinterpret_cast<uintptr_t>(W) & 15) == 0) && ((reinterpret_cast<uintptr_t>(O) & 15) == 0);
-    for (long long t = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; t < nblk;
-         t += static_cast<long long>(gridDim.x) * kThreads) {
-        const long long blk = blk_first + t;
-        uint32_t c[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(static_cast<unsigned long long>(blk) >> 32),
-                         s0, s1};
-        philox4x32_10(c, k0, k1);
-        const long long i0 = blk * 8 - base;  // local index of global index 8 blk
-        if (fast) {
-            // Eight elements of one row: 16-byte loads and store.
-            const long long r = i0 / C, col = i0 - r * C;
+    const long long stride = static_cast<long long>(gridDim.x) * kThreads;  // blocks per grid stride
+    long long t = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+    if (fast) {
+        // Whole blocks of eight elements of one row (base and C are multiples
+        // of 8): 16-byte loads and store. The row of O is needed only for a
+        // strided O or per-row steps; it is then advanced by the stride's
+        // (rows, columns) instead of dividing per block.
+        const long long es = stride * 8;
+        const bool track = rs != nullptr || ld_o != C;
+        long long i0 = t * 8, r = 0, col = 0, dr = 0, dc = 0;
+        if (track) {
+            r = i0 / C;
+            col = i0 - r * C;
+            dr = es / C;
+            dc = es - dr * C;
+        }
+        for (; t < nblk; t += stride, i0 += es) {
+            const long long blk = blk_first + t;
+            uint32_t c[4] = {static_cast<uint32_t>(blk),
+                             static_cast<uint32_t>(static_cast<unsigned long long>(blk) >> 32), s0, s1};
+            philox4x32_10(c, k0, k1);
             const float stepv = rs ? rs[r] : step_all;
             const uint4 wraw = *reinterpret_cast<const uint4*>(W + i0);
-            const uint4 oraw = *reinterpret_cast<const uint4*>(O + r * ld_o + col);
+            const uint4 oraw = *reinterpret_cast<const uint4*>(O + (track ? r * ld_o + col : i0));
             const uint16_t* wv = reinterpret_cast<const uint16_t*>(&wraw);
             const __half* ov = reinterpret_cast<const __half*>(&oraw);
             uint32_t outv[4];
@@ -501,18 +512,33 @@ __global__ void __launch_bounds__(kThreads) muon_update_kernel(MatrixSet Ws, Mat
                 outv[e >> 1] = pair;
             }
             *reinterpret_cast<uint4*>(W + i0) = make_uint4(outv[0], outv[1], outv[2], outv[3]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const long long i = i0 + e;
-                if (i < 0 || i >= numel) continue;
-                const long long r = i / C, col = i - r * C;
-                const float stepv = rs ? rs[r] : step_all;
-                const float w = __uint_as_float(static_cast<uint32_t>(W[i]) << 16);
-                const float o = __half2float(O[r * ld_o + col]);
-                const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
-                W[i] = sr_bf16(wn, sr_draw(c, e));
+            if (track) {
+                col += dc;
+                r += dr;
+                if (col >= C) {
+                    col -= C;
+                    ++r;
+                }
             }
+        }
+        return;
+    }
+    for (; t < nblk; t += stride) {
+        const long long blk = blk_first + t;
+        uint32_t c[4] = {static_cast<uint32_t>(blk), static_cast<uint32_t>(static_cast<unsigned long long>(blk) >> 32),
+                         s0, s1};
+        philox4x32_10(c, k0, k1);
+        const long long i0 = blk * 8 - base;  // local index of global index 8 blk
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const long long i = i0 + e;
+            if (i < 0 || i >= numel) continue;
+            const long long r = i / C, col = i - r * C;
+            const float stepv = rs ? rs[r] : step_all;
+            const float w = __uint_as_float(static_cast<uint32_t>(W[i]) << 16);
+            const float o = __half2float(O[r * ld_o + col]);
+            const float wn = __fsub_rn(__fmul_rn(decay, w), __fmul_rn(stepv, o));
+            W[i] = sr_bf16(wn, sr_draw(c, e));
         }
     }
 }
@@ -704,10 +730,15 @@ int launch_bounded_wait_test(const DevStatus& first, const DevStatus& rest, int 
 
 int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o, const long long* base_dev,
                        long long base_scalar, int count, int R, int C, float lr, float wd, float scale,
-                       uint64_t seed, uint64_t step, cudaStream_t s, const float* row_step) {
+                       uint64_t seed, uint64_t step, int num_sms, cudaStream_t s, const float* row_step) {
     if (count <= 0 || static_cast<long long>(R) * C <= 0) return cudaSuccess;
+    // One thread per block of eight elements up to one resident wave (eight
+    // 256-thread blocks per SM) over all matrices; beyond that every thread
+    // strides through the matrix.
     const long long groups = static_cast<long long>(R) * C / 8 + 2;
-    return launch_pdl(muon_update_kernel, dim3(grid_for(groups, kThreads * 2), count), dim3(kThreads), s, W, O,
+    const long long wave = std::max(1LL, (8LL * std::max(1, num_sms) + count - 1) / count);
+    const int gx = static_cast<int>(std::max(1LL, std::min(std::min(wave, 65535LL), (groups + kThreads - 1) / kThreads)));
+    return launch_pdl(muon_update_kernel, dim3(gx, count), dim3(kThreads), s, W, O,
                       ld_o, base_dev, base_scalar, R, C, lr, wd, scale, row_step, static_cast<uint32_t>(seed),
                       static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(step),
                       static_cast<uint32_t>(step >> 32));

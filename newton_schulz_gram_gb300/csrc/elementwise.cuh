@@ -4,10 +4,35 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "gemm.cuh"
 #include "ptx.cuh"
 
 namespace gns {
+
+// A set of G matrices: either contiguous (base + g * stride) or a device
+// array of per-matrix pointers (ptrs != nullptr).
+struct MatrixSet {
+    const void* base;
+    long long stride;       // elements between matrices when contiguous
+    const void* const* ptrs;
+};
+
+// The Frobenius norm is summed in parts of norm_part_len(numel) elements
+// (the last one shorter), norm_parts(numel) per matrix: a function of the
+// matrix size only, so a matrix's scale never depends on its bucket.
+constexpr long long kNormPartElems = 16384;
+constexpr int kMaxNormParts = 8192;
+
+__host__ __device__ inline long long norm_part_len(long long numel) {
+    const long long even = (numel + kMaxNormParts - 1) / kMaxNormParts;
+    const long long len = (even + 3) & ~3LL;
+    return len > kNormPartElems ? len : kNormPartElems;
+}
+
+__host__ __device__ inline int norm_parts(long long numel) {
+    const long long len = norm_part_len(numel);
+    const long long p = (numel + len - 1) / len;
+    return static_cast<int>(p < 1 ? 1 : p);
+}
 
 // Norm, scale and cast of a bucket of G fp32 R x C matrices in one pass:
 //   [momentum only] M[g] <- mu M[g] + float(grads[g]) (in place, fp32),
@@ -46,7 +71,7 @@ int launch_momentum(const MatrixSet& M, const MatrixSet& Gr, long long numel, in
 // lr scale.
 int launch_muon_update(const MatrixSet& W, const MatrixSet& O, long long ld_o,
                        const long long* base_dev, long long base_scalar, int count, int R, int C,
-                       float lr, float wd, float scale, uint64_t seed, uint64_t step,
+                       float lr, float wd, float scale, uint64_t seed, uint64_t step, int num_sms,
                        cudaStream_t s, const float* row_step = nullptr);
 
 // NorMuon statistics (Dion3 Eq. 2), fp32: per row r of O[g] (fp16 R x C,

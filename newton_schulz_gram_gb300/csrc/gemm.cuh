@@ -8,23 +8,15 @@
 // lower triangle are computed and each is also written transposed into the
 // upper triangle.
 //
-// The work of a launch is a list of items in a fixed order: GEMM tiles and,
-// when the program starts from the caller's fp32 matrices, "prep" items that
-// compute the Frobenius norm (norm items) and write the scaled fp16 copy
-// (cast items) of each matrix. The prep items come first, round by round
-// (round r: the norm items of matrix r, then the cast items of matrix r - 1,
-// so a matrix is re-read for its cast while it is still in L2); the tiles
-// follow phase by phase, matrix by matrix. The producer and the MMA issuer
-// skip the prep items, so the first tiles start as soon as their matrices
-// are cast, while the epilogue warps finish the remaining prep items.
-//
-// Every item, once done, adds kEpiWarps * CG to its matrix's counter in
-// global memory (one release per epilogue warp of each CTA); the last norm
-// warp of a matrix also publishes the matrix's scale and adds one more. An
-// item that needs earlier items of its matrix first waits until the counter
-// reaches its target (acquire). Matrices thus pipeline through the phases
-// without a grid-wide barrier. Every dependency points to an earlier item of
-// the list, and every CTA walks its items in list order.
+// The work of a launch is a list of tiles, phase by phase, matrix by
+// matrix. CTAs (pairs) claim the tiles in list order from a ticket counter.
+// Every tile, once stored, adds kEpiWarps * CG to its matrix's counter in
+// global memory (one release per CTA, cumulative over its epilogue warps'
+// stores); a tile that needs the earlier phases of its matrix first waits
+// until the counter reaches its target (acquire). Matrices thus pipeline
+// through the phases without a grid-wide barrier. Every dependency points
+// to a tile with a smaller ticket, claimed by a running CTA, so every wait
+// ends whatever the residency of the grid.
 #pragma once
 
 #include <cstdint>
@@ -82,73 +74,18 @@ constexpr int kMaxMaps = 64;
 constexpr int kMaxProblems = 48;
 constexpr int kMaxPhases = 40;
 
-// A set of G matrices: either contiguous (base + g * stride) or a device
-// array of per-matrix pointers (ptrs != nullptr).
-struct MatrixSet {
-    const void* base;
-    long long stride;       // elements between matrices when contiguous
-    const void* const* ptrs;
-};
-
-// The Frobenius norm of a matrix is summed in parts of norm_part_len(numel)
-// elements (the last one shorter), norm_parts(numel) per matrix: a function
-// of the matrix size only, so a matrix's scale never depends on its bucket
-// or on the tile shape.
-constexpr long long kNormPartElems = 16384;
-constexpr int kMaxNormParts = 8192;
-
-__host__ __device__ inline long long norm_part_len(long long numel) {
-    const long long even = (numel + kMaxNormParts - 1) / kMaxNormParts;
-    const long long len = (even + 3) & ~3LL;
-    return len > kNormPartElems ? len : kNormPartElems;
-}
-
-__host__ __device__ inline int norm_parts(long long numel) {
-    const long long len = norm_part_len(numel);
-    const long long p = (numel + len - 1) / len;
-    return static_cast<int>(p < 1 ? 1 : p);
-}
-
-// The prep items of a program (Dion3 Algorithm 3, line 2, with the App. B.2.2
-// safety factor): for each of the G R x C fp32 matrices x_g,
-//   [momentum only] M_g <- mu M_g + float(grads_g) (in place, fp32),
-//   scale_g = 2^k_exp / (1.05 (||x_g||_F + 1e-7)),
-//   out_g (R x C, row stride ld_out) = fp16(scale_g x_g).
-// Norm item i of matrix g covers parts i * CG + rank (one part per CTA);
-// each epilogue warp w sums its slice of the part into
-// partial[g][part * kEpiWarps + w]. The warp that completes the matrix's
-// norm items sums all of its partials in a fixed order into scale[g]. Cast
-// item i re-reads the same slices, scales and stores them. A non-finite
-// norm raises GNS_ERR_NONFINITE.
-struct PrepDesc {
-    MatrixSet in;     // fp32 inputs, or the momentum M (updated in place)
-    MatrixSet grads;  // bf16 gradients when momentum != 0
-    float mu;
-    int momentum;
-    int R, C, k_exp, nparts;
-    long long numel, part_len;
-    __half* out;
-    long long ld_out, stride_out;
-    float* partial;  // [G][nparts * kEpiWarps] per-warp partial sums
-    float* scale;    // [G]
-    int items;       // norm items (= cast items) per matrix: ceil(nparts / CG); 0 = no prep
-};
-
-enum ItemKind : int { kItemTile = 0, kItemNorm = 1, kItemCast = 2 };
-
 // Epilogue warps of a CTA of the GEMM program (two per TMEM lane quarter);
-// each adds one counter signal per item.
+// each CTA adds kEpiWarps counter signals per tile.
 constexpr int kEpiWarps = 8;
 
-// One work item of the list a CTA walks (16 bytes). meta = kind | problem
-// << 2 | matrix g << 8. Tiles: problem p, matrix g, origin (m0, n0). Prep
-// items: matrix g, item index within the matrix in m0. `wait` is the matrix
-// counter value the item needs before it starts (0: none).
+// One tile record (16 bytes): meta = problem | matrix g << 8 (negative: the
+// end of the walk), the tile's origin (m0, n0), and `wait`, the matrix
+// counter value the tile needs before it starts (0: none).
 struct alignas(16) ProgItem {
     int meta;
     int wait;
-    int m0;  // tile row origin, or prep item index
-    int n0;  // tile column origin
+    int m0;
+    int n0;
 };
 
 // An output written by the epilogue: G row-major matrices, element (g, r, c)
@@ -183,21 +120,20 @@ struct GemmProblem {
 struct GemmPhaseDesc {
     int prob_begin, nprob;  // problems prob[prob_begin .. prob_begin + nprob)
     int tiles_per_matrix;   // over all its problems
-    int item_begin;         // list index of its first item (phase 0: of its round-interleaved range)
-    int wait;               // counter target of its tiles: signals of all earlier items of the matrix
+    int item_begin;         // ticket of its first tile
+    int wait;               // counter target of its tiles: signals of all earlier tiles of the matrix
 };
 
 struct alignas(128) GemmProgram {
     CUtensorMap maps[kMaxMaps];
     GemmProblem prob[kMaxProblems];
     GemmPhaseDesc phase[kMaxPhases];
-    PrepDesc prep;
     int* counters;       // [G] per-matrix signal counters, zero at launch; null when nothing waits
-    ProgItem* items;     // per-CTA item lists built by the kernel: CTA b uses items + 2 b cap
-    int item_cap;        // capacity of one list (>= ceil(total_items / clusters))
+    int* ticket;         // the launch's ticket counter, zero at launch
     DevStatus st;
     int nmaps, nprob, nphase, G, total_items;
     int direct_store;    // full-width, 32-byte aligned output blocks go straight from registers to memory
+    int lookahead;       // a CTA pair claims tile j once its producer has taken tile j - lookahead (1 .. 8)
 };
 
 // Host-side launcher (gemm_tc.cu). Tile shapes: cg = 1 and bn = 128 or 256
@@ -206,10 +142,7 @@ struct alignas(128) GemmProgram {
 // attribute; the kernel waits for the previous grid before reading its
 // operands. Returns a cudaError_t value.
 int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream);
-// Clusters (of cg CTAs) the launch of a program with total_items items uses,
-// and the item-list bytes it needs (two lists of item_cap items per CTA).
-int gemm_launch_clusters(int total_items, int bn, int cg, int num_sms);
-size_t gemm_item_bytes(int total_items, int bn, int cg, int num_sms, int* item_cap);
+
 int gemm_smem_bytes(int bn, int cg);
 // Tile walk of one matrix of an M x N problem: lower-triangle tiles if sym.
 // Returns tiles per matrix and sets *walk_n (tiles per row walked for

@@ -44,9 +44,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 static_assert(sizeof(GemmProgram) <= 32764, "kernel parameter block too large");
-constexpr int kDepWarp = 2 + kEpiWarps;       // the dependency warp follows the epilogue warps
-constexpr int kThreads = 32 * (kDepWarp + 1);  // producer, MMA, epilogue, dependency
-constexpr int kDepRing = 4;                    // tiles the dependency warp may run ahead
+constexpr int kSchedWarp = 2 + kEpiWarps;     // the scheduler warp follows the epilogue warps
+constexpr int kThreads = 32 * (kSchedWarp + 1);  // producer, MMA, epilogue, scheduler
+constexpr int kRing = 8;                         // tiles the scheduler may run ahead of the slowest role
 
 // Per-warp epilogue shared memory: three 2 KB slots of 32 rows x 64 bytes
 // (64-byte swizzle). Slots 0 and 1 receive, by TMA, the C addend of the
@@ -87,15 +87,12 @@ struct CtlProb {
     int mA, mB, mAt, mBt, mC;
 };
 constexpr int kCtlBytes = kMaxPhases * static_cast<int>(sizeof(CtlPhase)) + kMaxProblems * static_cast<int>(sizeof(CtlProb));
-// Shared words of the epilogue group: the per-warp values of a reduction,
-// a broadcast flag and the list lengths.
-constexpr int kEpiWords = 16;
-__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 5 + 2 * kEpiWarps + 2 * kDepRing; }
+__host__ __device__ constexpr int kNumBars(int stages) { return 2 * stages + 5 + 2 * kEpiWarps + 3 * kRing; }
 
 template <int BN, int CG>
 constexpr int smem_bytes() {
     return 1024 + Cfg<BN, CG>::STAGES * (BM * BK * 2 + (BN / CG) * BK * 2) + kEpiWarps * SBUF +
-           kNumBars(Cfg<BN, CG>::STAGES) * 8 + 16 + kCtlBytes + 4 * kEpiWords;
+           kNumBars(Cfg<BN, CG>::STAGES) * 8 + 16 + kCtlBytes + 16 + kRing * static_cast<int>(sizeof(ProgItem));
 }
 static_assert(smem_bytes<256, 2>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<128, 1>() <= 232448, "shared memory budget");
@@ -107,11 +104,10 @@ __host__ __device__ __forceinline__ int sym_row_tiles(int i, int tm, int bn, int
     return c < tiles_n ? c : tiles_n;
 }
 
-__host__ __device__ __forceinline__ int item_kind(const ProgItem& it) { return it.meta & 3; }
-__host__ __device__ __forceinline__ int item_prob(const ProgItem& it) { return (it.meta >> 2) & 63; }
+__host__ __device__ __forceinline__ int item_prob(const ProgItem& it) { return it.meta & 255; }
 __host__ __device__ __forceinline__ int item_matrix(const ProgItem& it) { return static_cast<int>(static_cast<unsigned>(it.meta) >> 8); }
-__host__ __device__ __forceinline__ ProgItem make_item(int kind, int p, int g, int wait, int m0, int n0) {
-    return ProgItem{kind | (p << 2) | (g << 8), wait, m0, n0};
+__host__ __device__ __forceinline__ ProgItem make_item(int p, int g, int wait, int m0, int n0) {
+    return ProgItem{p | (g << 8), wait, m0, n0};
 }
 
 // Tile t (0-based, in walk order) of matrix g in phase `s`: the problem it
@@ -151,33 +147,12 @@ __host__ __device__ ProgItem decode_tile(const CtlPhase& ph, const CtlProb* cpb,
         i = t / cpb[p].tiles_n;
         j = t - i * cpb[p].tiles_n;
     }
-    return make_item(kItemTile, p, g, ph.wait, i * TM, j * BN);
+    return make_item(p, g, ph.wait, i * TM, j * BN);
 }
 
-// Item w of the program's list. With prep items (q norm and q cast items per
-// matrix), the list starts with G + 1 rounds: round r holds the norm items of
-// matrix r (r < G), then the cast items of matrix r - 1 (1 <= r <= G). The
-// phases' tiles follow, phase by phase, matrix by matrix.
+// Tile w of the program's list: phase by phase, matrix by matrix.
 template <int BN, int CG>
-__host__ __device__ ProgItem decode_item(const CtlPhase* cph, const CtlProb* cpb, int nphase, int G, int q, int w) {
-    constexpr int spi = kEpiWarps * CG;  // counter signals per item
-    if (q > 0 && w < 2LL * q * G) {
-        // Rounds 1 .. G - 1 hold 2q items; round 0 holds q, round G holds q.
-        int r, o;
-        if (w < q) {
-            r = 0;
-            o = w;
-        } else {
-            r = 1 + (w - q) / (2 * q);
-            o = (w - q) - (r - 1) * 2 * q;
-        }
-        if (r < G) {
-            if (o < q) return make_item(kItemNorm, 0, r, 0, o, 0);
-            o -= q;
-        }
-        // Casts wait for every norm item of the matrix and its scale.
-        return make_item(kItemCast, 0, r - 1, q * spi + 1, o, 0);
-    }
+__host__ __device__ ProgItem decode_item(const CtlPhase* cph, const CtlProb* cpb, int nphase, int w) {
     int s = 0;
     while (s + 1 < nphase && w >= cph[s + 1].item_begin) ++s;
     const int local = w - cph[s].item_begin;
@@ -453,195 +428,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     }
 }
 
-// ------------------------------------------------------------ prep items
-//
-// Run by each epilogue warp on its own, with no barrier among the warps:
-// norm and cast item i of matrix g cover part i * CG + rank (one part per
-// CTA of the pair), and warp w of a CTA owns slice w of every 16384-element
-// chunk of the part: 2048 elements, lane l taking the float4 groups
-// l + 32 u (u = 0 .. 15). Every sum runs in a fixed order, so a matrix's
-// scale depends on its size only (not on the bucket or the tile shape).
-
-constexpr int kSliceElems = static_cast<int>(kNormPartElems / kEpiWarps);  // 2048
-constexpr int kSliceVec = kSliceElems / (4 * 32);                           // float4 per lane: 16
-static_assert(kSliceVec * 4 * 32 * kEpiWarps == kNormPartElems, "a chunk is kEpiWarps slices");
-
-__device__ __forceinline__ float* prep_f32(const MatrixSet& s, int g) {
-    return s.ptrs ? static_cast<float*>(const_cast<void*>(s.ptrs[g]))
-                  : static_cast<float*>(const_cast<void*>(s.base)) + static_cast<long long>(g) * s.stride;
-}
-
-__device__ __forceinline__ const __nv_bfloat16* prep_bf16(const MatrixSet& s, int g) {
-    return s.ptrs ? static_cast<const __nv_bfloat16*>(s.ptrs[g])
-                  : static_cast<const __nv_bfloat16*>(s.base) + static_cast<long long>(g) * s.stride;
-}
-
-__device__ __forceinline__ float4 momentum4(float4 m, uint2 graw, float mu) {
-    const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(&graw);
-    const float2 g01 = __bfloat1622float2(gb[0]);
-    const float2 g23 = __bfloat1622float2(gb[1]);
-    m.x = __fadd_rn(__fmul_rn(mu, m.x), g01.x);
-    m.y = __fadd_rn(__fmul_rn(mu, m.y), g01.y);
-    m.z = __fadd_rn(__fmul_rn(mu, m.z), g23.x);
-    m.w = __fadd_rn(__fmul_rn(mu, m.w), g23.y);
-    return m;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Norm item, one warp: the sum of squares of its slices of the part (after
-// the momentum update, which it stores) into partial[g][part * kEpiWarps + w];
-// then the warp's signal. The warp whose signal completes the matrix's norm
-// items (counter value q * spi - 1 before it) sums all of the matrix's
-// partials in a fixed order and publishes scale[g] with one more signal.
-static __device__ __noinline__ void prep_norm(const PrepDesc& d, int* counter, int done_target, const DevStatus& st,
-                                              int g, int part, int w, int lane) {
-    float s = 0.0f;
-    if (part < d.nparts) {
-        float* x = prep_f32(d.in, g);
-        const __nv_bfloat16* gr = d.momentum ? prep_bf16(d.grads, g) : nullptr;
-        const long long beg = static_cast<long long>(part) * d.part_len;
-        const long long end = beg + d.part_len < d.numel ? beg + d.part_len : d.numel;
-        for (long long c = beg; c < end; c += kNormPartElems) {
-            const long long sb = c + static_cast<long long>(w) * kSliceElems;  // this warp's slice
-            long long se = sb + kSliceElems;
-            if (se > end) se = end;
-            if (sb >= se) continue;
-            const bool full = se - sb == kSliceElems && (reinterpret_cast<uintptr_t>(x + sb) & 15) == 0 &&
-                              (!gr || (reinterpret_cast<uintptr_t>(gr + sb) & 7) == 0);
-            if (full) {
-                float4* xv = reinterpret_cast<float4*>(x + sb) + lane;
-                float4 r[kSliceVec];
-                if (gr) {
-                    const uint2* gv = reinterpret_cast<const uint2*>(gr + sb) + lane;
-                    uint2 gg[kSliceVec];
-#pragma unroll
-                    for (int u = 0; u < kSliceVec; ++u) {
-                        r[u] = __ldcg(xv + 32 * u);
-                        gg[u] = __ldcg(gv + 32 * u);
-                    }
-#pragma unroll
-                    for (int u = 0; u < kSliceVec; ++u) {
-                        r[u] = momentum4(r[u], gg[u], d.mu);
-                        __stcg(xv + 32 * u, r[u]);
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < kSliceVec; ++u) r[u] = __ldcg(xv + 32 * u);
-                }
-#pragma unroll
-                for (int u = 0; u < kSliceVec; ++u) {
-                    s = fmaf(r[u].x, r[u].x, s);
-                    s = fmaf(r[u].y, r[u].y, s);
-                    s = fmaf(r[u].z, r[u].z, s);
-                    s = fmaf(r[u].w, r[u].w, s);
-                }
-            } else {
-                for (long long i = sb + 4LL * lane; i < se; i += 128) {
-                    for (int e = 0; e < 4; ++e) {
-                        if (i + e < se) {
-                            float v = __ldcg(x + i + e);
-                            if (gr) {
-                                v = __fadd_rn(__fmul_rn(d.mu, v), __bfloat162float(gr[i + e]));
-                                __stcg(x + i + e, v);
-                            }
-                            s = fmaf(v, v, s);
-                        }
-                    }
-                }
-            }
-        }
-    }
-    s = warp_sum(s);
-    __syncwarp();  // every lane's stores precede lane 0's release below
-    int last = 0;
-    if (lane == 0) {
-        if (part < d.nparts) d.partial[(static_cast<long long>(g) * d.nparts + part) * kEpiWarps + w] = s;
-        if (counter) {
-            // The signal with acquire-release: the warp that completes the
-            // norm items sees every other warp's partial.
-            const int old = atom_add_acqrel_gpu(counter, 1);
-            last = old == done_target - 1;
-        }
-    }
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __syncwarp();  // lane 0's acquire precedes every lane's reads below
-    // The matrix's scale from all of its partials, in a fixed order.
-    const long long np = static_cast<long long>(d.nparts) * kEpiWarps;
-    const float* pp = d.partial + static_cast<long long>(g) * np;
-    float v = 0.0f;
-    for (long long k = lane; k < np; k += 32) v += __ldcg(pp + k);
-    v = warp_sum(v);
-    if (lane == 0) {
-        const float norm = sqrtf(v);
-        if (!isfinite(norm)) raise_error(st, kDevErrNonFinite);
-        d.scale[g] = ldexpf(1.0f, d.k_exp) / (1.05f * (norm + 1e-7f));
-        red_release_add(counter, 1);
-    }
-    __syncwarp();
-}
-
-// Cast item, one warp: once the matrix's scale is published (its counter
-// reached `wait`), this warp's slices of the part scaled and stored in fp16.
-// Returns false when the wait gave up.
-static __device__ __noinline__ bool prep_cast(const PrepDesc& d, const int* counter, int wait, const DevStatus& st,
-                                              int g, int part, int w, int lane) {
-    int ok = 1;
-    if (lane == 0 && counter) ok = wait_counter(counter, wait, st) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-    __syncwarp();  // lane 0's acquire precedes every lane's reads below
-    if (part >= d.nparts) return true;
-    const float scale = __ldcg(d.scale + g);
-    const float* x = prep_f32(d.in, g);
-    __half* out = d.out + static_cast<long long>(g) * d.stride_out;
-    const int C = d.C;
-    const long long ld = d.ld_out;
-    const long long beg = static_cast<long long>(part) * d.part_len;
-    const long long end = beg + d.part_len < d.numel ? beg + d.part_len : d.numel;
-    auto h4 = [&](float4 f) {
-        __half2 h01 = __floats2half2_rn(f.x * scale, f.y * scale);
-        __half2 h23 = __floats2half2_rn(f.z * scale, f.w * scale);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t*>(&h01);
-        packed.y = *reinterpret_cast<uint32_t*>(&h23);
-        return packed;
-    };
-    for (long long c = beg; c < end; c += kNormPartElems) {
-        const long long sb = c + static_cast<long long>(w) * kSliceElems;
-        long long se = sb + kSliceElems;
-        if (se > end) se = end;
-        if (sb >= se) continue;
-        if (se - sb == kSliceElems && (reinterpret_cast<uintptr_t>(x + sb) & 15) == 0 && C % 4 == 0) {
-            const float4* xv = reinterpret_cast<const float4*>(x + sb) + lane;
-            float4 r[kSliceVec];
-#pragma unroll
-            for (int u = 0; u < kSliceVec; ++u) r[u] = __ldcg(xv + 32 * u);
-            if (ld == C) {
-                uint2* o = reinterpret_cast<uint2*>(out + sb) + lane;
-#pragma unroll
-                for (int u = 0; u < kSliceVec; ++u) o[32 * u] = h4(r[u]);
-            } else {
-#pragma unroll
-                for (int u = 0; u < kSliceVec; ++u) {
-                    const long long i = sb + 4LL * (lane + 32 * u);
-                    const long long row = i / C;
-                    *reinterpret_cast<uint2*>(out + row * ld + (i - row * C)) = h4(r[u]);
-                }
-            }
-        } else {
-            for (long long i = sb + lane; i < se; i += 32) {
-                const long long row = i / C;
-                out[row * ld + (i - row * C)] = __float2half_rn(__ldcg(x + i) * scale);
-            }
-        }
-    }
-    return true;
-}
-
 template <int BN, int CG>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmProgram P) {
     constexpr int CL = CG;  // CTAs per cluster: one pair, or one CTA
@@ -664,8 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t pub0 = smem_u32(tmem_slot + 2);  // per-buffer counts of finished epilogue warps
     CtlPhase* cph = reinterpret_cast<CtlPhase*>(tmem_slot + 4);
     CtlProb* cpb = reinterpret_cast<CtlProb*>(cph + kMaxPhases);
-    float* red = reinterpret_cast<float*>(cpb + kMaxProblems);  // kEpiWords shared words
-    int* list_len = reinterpret_cast<int*>(red + kEpiWords - 2);  // [0] all items, [1] tiles
+    // kRing tile records, 16-byte aligned (vector accesses, also from the peer CTA).
+    ProgItem* ring =
+        reinterpret_cast<ProgItem*>((reinterpret_cast<uintptr_t>(cpb + kMaxProblems) + 15) & ~uintptr_t(15));
 
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
@@ -673,9 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t acce0 = smem_u32(bars + 2 * STAGES + 2);
     const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
     const uint32_t cbar0 = smem_u32(bars + 2 * STAGES + 5);  // two C-slot barriers per epilogue warp
-    // Dependency ring: slot j's "ready" and "free" barriers.
-    const uint32_t depf0 = smem_u32(bars + 2 * STAGES + 5 + 2 * kEpiWarps);
-    const uint32_t depe0 = depf0 + 8 * kDepRing;
+    // Tile ring: slot j's "record ready" barrier (in every CTA) and "free"
+    // barrier (the pair leader's, counting every consumer of both CTAs).
+    const uint32_t ringf0 = smem_u32(bars + 2 * STAGES + 5 + 2 * kEpiWarps);
+    const uint32_t ringe0 = ringf0 + 8 * kRing;
+    // Slot j's "taken by the producer" barrier (the pair leader's producer):
+    // paces the claims (the program's lookahead).
+    const uint32_t taken0 = ringe0 + 8 * kRing;
+    constexpr int kRingConsumers = CG * (1 + kEpiWarps) + 1;  // producers, epilogue warps, MMA issuer
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -683,14 +475,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0;  // rank in the cluster
     const uint32_t rank = crank & (CG - 1);                  // rank in the pair: 0 = leader
     const uint32_t lead = crank & ~uint32_t(CG - 1);         // cluster rank of the pair leader
-    const int unit = blockIdx.x / CL;                        // this cluster's position in the walk
-    const int units = gridDim.x / CL;
     const int nphase = P.nphase;
-    const int G = P.G;
-    // This CTA's item lists: all of its cluster's items in order (epilogue),
-    // and the tiles among them (producer and MMA issuer).
-    ProgItem* ep_items = P.items + static_cast<size_t>(blockIdx.x) * 2 * P.item_cap;
-    ProgItem* mm_items = ep_items + P.item_cap;
+    const uint32_t ring_u32 = smem_u32(ring);
+    const uint32_t ringe_lead = (CG == 2) ? map_to_rank(ringe0, lead) : ringe0;
+    // Reads the record of ring slot j once its "ready" phase is complete and
+    // hands the slot back; returns false when the wait gave up.
+    auto take = [&](int j, ProgItem& out) -> bool {
+        const int slot = j % kRing;
+        if (!mbar_wait_cluster(ringf0 + 8 * slot, (j / kRing) & 1, err)) return false;
+        out = ring[slot];
+        if constexpr (CG == 2)
+            mbar_arrive_cluster(ringe_lead + 8 * slot);
+        else
+            mbar_arrive(ringe0 + 8 * slot);
+        return true;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -703,9 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         mbar_init(drain_bar, 1);
         for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(cbar0 + 8 * b, 1);
-        for (int b = 0; b < kDepRing; ++b) {
-            mbar_init(depf0 + 8 * b, 1);
-            mbar_init(depe0 + 8 * b, 1);
+        for (int b = 0; b < kRing; ++b) {
+            mbar_init(ringf0 + 8 * b, 1);
+            mbar_init(ringe0 + 8 * b, kRingConsumers);
+            mbar_init(taken0 + 8 * b, 1);
         }
         tmem_slot[2] = 0;
         tmem_slot[3] = 0;
@@ -727,51 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         tmem_alloc<CG>(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish<CG>();
     }
-    __syncthreads();
-    {
-        // Build this CTA's item lists: items unit, unit + units, ... of the
-        // program. Each thread decodes a contiguous range of them; a scan of
-        // the per-thread tile counts places the tiles. The lists belong to
-        // this launch alone (launches alternate between two list regions), so
-        // this overlaps the previous kernel's tail.
-        const int n_mine = P.total_items > unit ? (P.total_items - unit + units - 1) / units : 0;
-        const int per = (n_mine + kThreads - 1) / kThreads;
-        const int k0 = threadIdx.x * per < n_mine ? threadIdx.x * per : n_mine;
-        const int k1 = k0 + per < n_mine ? k0 + per : n_mine;
-        int cnt = 0;
-        for (int k = k0; k < k1; ++k) {
-            const ProgItem it = decode_item<BN, CG>(cph, cpb, nphase, G, P.prep.items, unit + k * units);
-            ep_items[k] = it;
-            cnt += item_kind(it) == kItemTile;
-        }
-        // Exclusive scan of cnt over the block's threads (warp scan, then the warp totals).
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int* wsum = reinterpret_cast<int*>(red);  // kThreads / 32 <= kEpiWords - 2 words
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        int off = incl - cnt;
-        for (int w = 0; w < warp; ++w) off += wsum[w];
-        if (threadIdx.x == kThreads - 1) {
-            list_len[0] = n_mine;
-            list_len[1] = off + cnt;
-        }
-        for (int k = k0; k < k1; ++k) {
-            const ProgItem it = ep_items[k];
-            if (item_kind(it) == kItemTile) mm_items[off++] = it;
-        }
-    }
     tc_fence_before();
     __syncthreads();
     if constexpr (CL > 1) cluster_sync();  // all CTAs' barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int n_items = list_len[0];
-    const int n_tiles = list_len[1];
     // Everything above overlaps the previous kernel's tail; operands written
     // by it are read only after this point.
     grid_dependency_wait();
@@ -783,10 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t stage = 0, phase = 0;
             int issued = 0;
             bool ok = true;
-            ProgItem nxt = n_tiles > 0 ? mm_items[0] : ProgItem{};
-            for (int k = 0; k < n_tiles && ok; ++k) {
-                const ProgItem it = nxt;
-                if (k + 1 < n_tiles) nxt = mm_items[k + 1];
+            for (int k = 0; ok; ++k) {
+                ProgItem it;
+                if (!take(k, it) || it.meta < 0) break;
+                if (rank == 0) mbar_arrive(taken0 + 8 * (k % kRing));
                 const int g = item_matrix(it);
                 const CtlProb& pr = cpb[item_prob(it)];
                 const CUtensorMap* mapA = &P.maps[pr.mA];
@@ -799,16 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const CUtensorMap* mapBt = b_sym ? &P.maps[pr.mBt] : mapB;
                 const int ti = it.m0 / TM, tj = it.n0 / TM;
                 const int kblocks = (pr.K + BK - 1) / BK;
-                {
-                    // The operands of this tile are outputs of earlier items on
-                    // the same matrix, stored by other CTAs: the dependency
-                    // warp has acquired them (its release on the ring slot
-                    // orders that acquire before these loads).
-                    const int slot = k % kDepRing;
-                    if (!mbar_wait(depf0 + 8 * slot, (k / kDepRing) & 1, err)) break;
-                    mbar_arrive(depe0 + 8 * slot);
-                    if (it.wait > 0) fence_proxy_async_global();
-                }
+                // The operands of this tile are outputs of earlier tiles on the
+                // same matrix, stored by other CTAs: the scheduler acquired
+                // them before it published the tile (its release on the ring
+                // orders that acquire before these loads).
+                if (it.wait > 0) fence_proxy_async_global();
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, err)) {
                         ok = false;
@@ -869,10 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             // byte offset / 16 to the start-address field (addresses < 256 KB).
             const uint64_t ak0 = sw128_kmajor_desc(smem_u32(sA)), amn0 = sw128_mnmajor_desc(smem_u32(sA), kMnBlockBytes);
             const uint64_t bk0 = sw128_kmajor_desc(smem_u32(sB)), bmn0 = sw128_mnmajor_desc(smem_u32(sB), kMnBlockBytes);
-            ProgItem nxt = n_tiles > 0 ? mm_items[0] : ProgItem{};
-            for (int k = 0; k < n_tiles && ok; ++k) {
-                const ProgItem it = nxt;
-                if (k + 1 < n_tiles) nxt = mm_items[k + 1];
+            for (int k = 0; ok; ++k) {
+                ProgItem it;
+                if (!take(k, it) || it.meta < 0) break;
                 const CtlProb& pr = cpb[item_prob(it)];
                 const int pflags = pr.flags;
                 const int kblocks = (pr.K + BK - 1) / BK;
@@ -925,18 +679,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             drain_wait(drain_bar, 0, err.limit_ns);
         }
         __syncwarp();
-    } else if (warp == kDepWarp) {
-        // ----------------------------------------------------- dependencies
-        // Acquires each tile's dependency (the counter of its matrix) up to
-        // kDepRing tiles ahead of the producer, so that the producer's loads
-        // never wait for an acquire's round trip to memory.
-        if (lane == 0) {
-            for (int k = 0; k < n_tiles; ++k) {
-                const int slot = k % kDepRing;
-                if (!mbar_wait(depe0 + 8 * slot, ((k / kDepRing) & 1) ^ 1, err)) break;
-                const ProgItem it = mm_items[k];
-                if (P.counters && it.wait > 0 && !wait_counter(P.counters + item_matrix(it), it.wait, err)) break;
-                mbar_arrive(depf0 + 8 * slot);
+    } else if (warp == kSchedWarp) {
+        // ------------------------------------------------------- scheduler
+        // The pair leader's scheduler claims the pair's next tile from the
+        // launch's ticket counter, decodes it, acquires its inputs (its
+        // matrix's counter) and publishes the record in the ring slot of both
+        // CTAs. A slot is reused once every role of both CTAs has read it; a
+        // tile is claimed only `lookahead` tiles ahead of the producer, so a
+        // pair never holds tiles (long ones of the first phase above all)
+        // that another pair would start sooner. Claiming in ticket order
+        // makes every wait end whatever the residency of the grid: a tile
+        // waits only for tiles with smaller tickets, claimed by running CTAs.
+        // A record with meta < 0 ends the walk.
+        if (lane == 0 && rank == 0) {
+            const uint32_t peer_ring = (CG == 2) ? map_to_rank(ring_u32, lead + 1) : 0;
+            const uint32_t peer_ringf = (CG == 2) ? map_to_rank(ringf0, lead + 1) : 0;
+            const int la = P.lookahead < 1 ? 1 : (P.lookahead > kRing ? kRing : P.lookahead);
+            for (int j = 0;; ++j) {
+                const int slot = j % kRing;
+                if (!mbar_wait_cluster(ringe0 + 8 * slot, ((j / kRing) & 1) ^ 1, err)) break;
+                // Tile j is claimed once the producer has taken tile j - la.
+                // The producer has taken at most j - 1 tiles and la <= kRing,
+                // so the slot's barrier is at most one phase ahead.
+                if (j >= la && !mbar_wait(taken0 + 8 * ((j - la) % kRing), ((j - la) / kRing) & 1, err)) break;
+                const int t = atomicAdd(P.ticket, 1);
+                ProgItem rec{-1, 0, 0, 0};
+                if (t < P.total_items) {
+                    rec = decode_item<BN, CG>(cph, cpb, nphase, t);
+                    if (P.counters && rec.wait > 0 &&
+                        !wait_counter(P.counters + item_matrix(rec), rec.wait, err))
+                        break;
+                }
+                ring[slot] = rec;
+                mbar_arrive(ringf0 + 8 * slot);
+                if constexpr (CG == 2) {
+                    st_cluster_v4(peer_ring + slot * static_cast<uint32_t>(sizeof(ProgItem)), rec.meta, rec.wait,
+                                  rec.m0, rec.n0);
+                    mbar_arrive_cluster(peer_ringf + 8 * slot);
+                }
+                if (rec.meta < 0) break;
             }
         }
         __syncwarp();
@@ -954,27 +735,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         uint32_t cpend = 0; // bit k: a C load into slot k is in flight
         int iter = 0;       // GEMM tiles done (accumulator buffer iter & 1)
         bool ok = true;
-        ProgItem nxt = n_items > 0 ? ep_items[0] : ProgItem{};
-        for (int k = 0; k < n_items && ok; ++k) {
-            const ProgItem it = nxt;
-            if (k + 1 < n_items) nxt = ep_items[k + 1];
-            const int kind = item_kind(it);
-            const int g = item_matrix(it);
-            if (kind != kItemTile) {
-                // Norm or cast item: each epilogue warp handles its own slice.
-                const int part = it.m0 * CG + static_cast<int>(rank);
-                int* counter = P.counters ? P.counters + g : nullptr;
-                if (kind == kItemNorm) {
-                    // The norm signals of a matrix: kEpiWarps per CTA per item.
-                    prep_norm(P.prep, counter, P.prep.items * kEpiWarps * CG, err, g, part, ew, lane);
-                } else {
-                    if (!prep_cast(P.prep, counter, it.wait, err, g, part, ew, lane)) break;
-                    // Every lane's stores precede lane 0's release.
-                    __syncwarp();
-                    if (lane == 0 && counter) red_release_add(counter, 1);
-                }
-                continue;
+        for (int k = 0; ok; ++k) {
+            // The tile record: lane 0 waits for the slot and hands it back
+            // once every lane holds the record.
+            ProgItem it{};
+            int got = 0;
+            const int slot = k % kRing;
+            if (lane == 0) got = mbar_wait_cluster(ringf0 + 8 * slot, (k / kRing) & 1, err) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, got, 0)) break;
+            __syncwarp();
+            it = ring[slot];
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 2)
+                    mbar_arrive_cluster(ringe_lead + 8 * slot);
+                else
+                    mbar_arrive(ringe0 + 8 * slot);
             }
+            if (it.meta < 0) break;
+            const int g = item_matrix(it);
             const GemmProblem& pr = P.prob[item_prob(it)];
             const int buf = iter & 1;
             const int flags = cpb[item_prob(it)].flags;
@@ -1206,9 +985,10 @@ int max_clusters(VariantState& vs, int num_sms) {
     }
     if (vs.clusters < 0) {
         cudaGetLastError();
-        return num_sms / CG;
+        return num_sms / CG > 1 ? num_sms / CG : 1;
     }
-    return vs.clusters < num_sms / CG ? vs.clusters : num_sms / CG;
+    const int cap = num_sms / CG > 1 ? num_sms / CG : 1;  // at least one cluster, even under an SM cap of 1
+    return vs.clusters < cap ? vs.clusters : cap;
 }
 
 template <int BN, int CG>
@@ -1224,8 +1004,6 @@ int launch_impl(const GemmProgram& prog, int num_sms, cudaStream_t stream) {
     if (prog.total_items <= 0) return cudaSuccess;
     const int clusters = max_clusters<BN, CG>(vs, num_sms);
     const int grid = CG * (prog.total_items < clusters ? prog.total_items : clusters);
-    // Every CTA's two lists must fit the capacity the host planned for.
-    if (static_cast<long long>(prog.item_cap) * (grid / CG) < prog.total_items) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -1265,29 +1043,6 @@ int gemm_tiles_per_matrix(int M, int N, int bn, int cg, bool sym, int* walk_n) {
 }
 
 int gemm_signals_per_tile(int cg) { return kEpiWarps * cg; }
-
-int gemm_launch_clusters(int total_items, int bn, int cg, int num_sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
-        return num_sms / cg;
-    }
-    int clusters;
-    if (cg == 2)
-        clusters = max_clusters<256, 2>(variant_state<256, 2>(dev), num_sms);
-    else if (bn == 256)
-        clusters = max_clusters<256, 1>(variant_state<256, 1>(dev), num_sms);
-    else
-        clusters = max_clusters<128, 1>(variant_state<128, 1>(dev), num_sms);
-    return total_items < clusters ? total_items : clusters;
-}
-
-size_t gemm_item_bytes(int total_items, int bn, int cg, int num_sms, int* item_cap) {
-    const int clusters = gemm_launch_clusters(total_items, bn, cg, num_sms);
-    const int cap = clusters > 0 ? (total_items + clusters - 1) / clusters : 0;
-    if (item_cap) *item_cap = cap;
-    return static_cast<size_t>(clusters) * cg * 2 * static_cast<size_t>(cap) * sizeof(ProgItem);
-}
 
 int launch_gemm_program(const GemmProgram& prog, int bn, int cg, int num_sms, cudaStream_t stream) {
     if (cg == 2) return launch_impl<256, 2>(prog, num_sms, stream);

@@ -89,6 +89,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with acquire semantics at cluster scope: for phases completed by
+// arrivals from other CTAs of the cluster that publish data.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity, const DevStatus& st) {
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (call_aborted(st)) return false;
+        if (globaltimer() - t0 > st.limit_ns) {
+            raise_timeout(st);
+            return false;
+        }
+    }
+}
+
+// Bounded wait with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const DevStatus& st) {
+    return mbar_try_wait_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity, st);
+}
+
 // The bounded spin of mbar_wait, out of line.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const DevStatus& st) {
     const uint64_t t0 = globaltimer();
@@ -169,6 +201,13 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
+}
+
+// 16 bytes into the shared memory of a CTA of the cluster (a shared::cluster
+// address).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, int a, int b, int c, int d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
 }
 
 // Arrive on an mbarrier that may live in another CTA of the cluster.
