@@ -1,7 +1,8 @@
-// HBM-bound kernels around the GEMM core: the Muon elementwise passes (the
-// standalone momentum and update kernels), the NorMuon statistics, the copy
-// of unaligned outputs and the bounded-wait check. (The norm, scale and fp16
-// cast of the inputs run as the first items of the GEMM program.)
+// HBM-bound kernels around the GEMM core: the norm, scale and fp16 cast of
+// the inputs (with the Muon momentum update first, for the Muon step), the
+// Muon elementwise passes (the standalone momentum and update kernels), the
+// NorMuon statistics, the copy of unaligned outputs and the bounded-wait
+// check.
 //
 // Arithmetic contracts (shared with nothing else; restated from the pages):
 // * Momentum (Dion3 Eq. 1): M <- mu M + G, fp32, two roundings.
