@@ -378,6 +378,36 @@ def llama7b_line(gns, torch, stream, dev, peaks):
                 "muon_update_kernel": upd}}
 
 
+def muon_bucket_line(gns, torch, stream, dev, G_, blocks):
+    """muon_step over G_ parameters of R x C (the benchmark's matrix shape):
+    bf16 W ~ N(0, 0.02), bf16 G ~ N(0, 1e-3), fp32 M, drawn on the device.
+    One call is the momentum + norm + cast pass and the GEMM program with the
+    update fused into its last product's epilogue."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(5000)
+    W = [(0.02 * torch.randn(R, C, device=dev, generator=g)).to(torch.bfloat16) for _ in range(G_)]
+    Gr = [(1e-3 * torch.randn(R, C, device=dev, generator=g)).to(torch.bfloat16) for _ in range(G_)]
+    M = [1e-3 * torch.randn(R, C, device=dev, generator=g) for _ in range(G_)]
+    step = [2]
+
+    def one():
+        gns.muon_step(W, Gr, M, lr=0.02, wd=0.01, mu=0.95, seed=0, step=step[0])
+        step[0] += 1
+
+    one()
+    torch.cuda.synchronize()
+    gns.gns_profile_enable(True)
+    gns.gns_profile_read()
+    ms, q = time_calls(torch, stream, one, calls=1, warmup=2, blocks=blocks)
+    gns.gns_profile_enable(False)
+    prof = gns.gns_profile_read()
+    if gns.gns_get_status() != 0:
+        raise SystemExit("device status error in muon_step")
+    calls = blocks + 2
+    return {"workload": f"muon_step over {G_} x {R}x{C}", "ms_per_step": ms, "ms_quartiles": q,
+            "kernels_ms_per_step": {k: t / calls for k, (n, t) in prof.items() if n}}
+
+
 def update_rate(gns, torch, stream, dev, log2n, peaks, blocks=10):
     """The standalone update kernel (W <- SR_bf16(decay W - step O)) over
     2^log2n elements of a square matrix: W read and written, O read, 6 B per
@@ -436,9 +466,20 @@ def main():
     ap.add_argument("--traffic-matrices", type=int, default=12, help="matrices in the captured launch")
     ap.add_argument("--only-update", type=int, metavar="LOG2N",
                     help="time only the standalone Muon update kernel on 2^LOG2N elements, print its rate and exit")
+    ap.add_argument("--only-muon", type=int, metavar="G",
+                    help="time only muon_step over G parameters of 1024 x 4096 (update fused into the GEMM "
+                         "program's epilogue), print the step time and exit")
     args = ap.parse_args()
     if args.record_traffic:
         return record_traffic(args.record_traffic, args.traffic_matrices)
+    if args.only_muon:
+        import torch
+        import newton_schulz_gram_gb300 as gns
+        gns.load()
+        dev = torch.device("cuda", 0)
+        print(json.dumps(muon_bucket_line(gns, torch, torch.cuda.current_stream(dev), dev, args.only_muon,
+                                          max(3, args.steps // 4))))
+        return
     if args.only_update:
         import torch
         import newton_schulz_gram_gb300 as gns

@@ -84,6 +84,34 @@ int gns_orthogonalize_batched_schedule(float* ptr, int G, int R, int C, int step
                                        const float* coeffs, void* stream);
 
 /*
+ * gns_gram_ns_state: gns_orthogonalize_batched on a rectangular bucket that
+ * also hands back the iteration's fp16 Gram state, to check the stability
+ * bounds of Dion3 App. B.2.1 (Fig. 18: with a restart after step 2 the
+ * eigenvalues of R_t stay above -0.4 and those of Q_t below about 100).
+ *
+ *   ptr, G, R, C, steps, restart_mask  as gns_orthogonalize_batched_schedule
+ *              (bit t: restart after step t), with R != C (square matrices
+ *              have no Gram state: GNS_ERR_INVALID) and the whole bucket in
+ *              one workspace chunk (else GNS_ERR_INVALID). Default
+ *              coefficients.
+ *   r_state    device uint16 (fp16 bits) [G][n][n], n = min(R, C): the last
+ *              Gram matrix R the run computed (R_{steps-1}, or X X^T when a
+ *              restart follows the last update; R_0 for steps = 1), scaled:
+ *              stored R = r_scale * R. Only the lower triangle (with the
+ *              diagonal) is defined: the library stores symmetric
+ *              intermediates lower-only.
+ *   q_state    device uint16 (fp16 bits) [G][n][n]: the final Q_steps (the
+ *              accumulated polynomial since the last restart), unscaled,
+ *              lower triangle defined as for r_state.
+ *   r_scale    HOST float: receives the power-of-two state scale.
+ *   stream     cudaStream_t. The copies are stream-ordered after the run.
+ * Returns GNS_OK or a negative gns_status. Diagnostic: it runs the same
+ * program as gns_orthogonalize_batched plus two device copies.
+ */
+int gns_gram_ns_state(float* ptr, int G, int R, int C, int steps, uint64_t restart_mask, uint16_t* r_state,
+                      uint16_t* q_state, float* r_scale, void* stream);
+
+/*
  * gns_orthogonalize_batched_host: the same computation on a HOST buffer.
  * host_ptr is fp32 [G][R][C] in host memory (pinned memory gives full copy
  * speed); the library copies it to a device staging buffer it owns, runs

@@ -80,6 +80,27 @@ def gns_orthogonalize_batched_schedule(x, steps=5, restarts=(2,), coeffs=None, s
     return x
 
 
+def gns_gram_ns_state(x, steps=5, restarts=(2,), stream=None):
+    """Orthogonalize the rectangular bucket x in place (restart after each
+    step in `restarts`) and return the iteration's final Gram state:
+    (r_state, q_state, r_scale), two fp16 [G, n, n] device tensors (lower
+    triangles defined) with stored R = r_scale * R, and Q unscaled."""
+    _require(x, torch.float32, name="x")
+    G, R, C = (1, *x.shape) if x.dim() == 2 else tuple(x.shape)
+    n = min(R, C)
+    r_state = torch.empty(G, n, n, dtype=torch.float16, device=x.device)
+    q_state = torch.empty(G, n, n, dtype=torch.float16, device=x.device)
+    scale = ctypes.c_float(0.0)
+    mask = 0
+    for t in restarts:
+        mask |= 1 << int(t)
+    lib = load()
+    check(lib.gns_gram_ns_state(ctypes.c_void_p(x.data_ptr()), G, R, C, steps, mask,
+                                ctypes.c_void_p(r_state.data_ptr()), ctypes.c_void_p(q_state.data_ptr()),
+                                ctypes.byref(scale), _stream(stream, x.device)), "gns_gram_ns_state")
+    return r_state, q_state, float(scale.value)
+
+
 def gns_orthogonalize_batched_host(x, steps=5, restart_at=2, coeffs=None, stream=None):
     """The same on a host fp32 tensor (pinned memory copies fastest); synchronous."""
     _require(x, torch.float32, cuda=False, name="x")

@@ -26,6 +26,7 @@ PROTOTYPES = {
     "gns_orthogonalize_batched": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "gns_orthogonalize_batched_schedule": (_i, [_vp, _i, _i, _i, _i, _u64, _vp, _vp]),
     "gns_orthogonalize_batched_host": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "gns_gram_ns_state": (_i, [_vp, _i, _i, _i, _i, _u64, _vp, _vp, ctypes.POINTER(ctypes.c_float), _vp]),
     "gns_orthogonalize_batched_noalloc": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "muon_step": (_i, [ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor), ctypes.POINTER(GnsTensor),
                        _i, _f, _f, _f, _u64, _u64, _vp]),

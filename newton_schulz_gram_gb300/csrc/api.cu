@@ -658,11 +658,21 @@ Mat mat16(char* ws, size_t off, int rows, int cols, long long ld) {
     return m;
 }
 
+// Where a run left its Gram state (rectangular buckets): the last R it
+// computed and the final Q, each Gc fp16 n x n matrices (row stride ld,
+// matrix stride stride, elements); stored R = s R (s = 4^k), Q unscaled.
+struct GramState {
+    const void* r = nullptr;
+    const void* q = nullptr;
+    long long ld = 0, stride = 0;
+    float s = 1.0f;
+};
+
 // Runs the orthogonalization of one chunk of Gc fp32 matrices `in` (the
 // momentum, first updated in place as M <- mu M + G, when grads is given).
 int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, const MatrixSet& in,
              const MatrixSet* grads, float mu, int steps, uint64_t restarts, const Coeffs& cf, const OutSpec& os,
-             cudaStream_t s) {
+             cudaStream_t s, GramState* state = nullptr) {
     const TileShape ts = choose_tile(g.n, Gc, st.num_sms);
     char* ws = st.ws;
     ProgramBuilder prog(st, Gc, ts, reinterpret_cast<int*>(ws + L.sync), s);
@@ -869,6 +879,13 @@ int run_core(DeviceState& st, const BucketGeom& g, const Layout& L, int Gc, cons
             p.a_sym = p.b_sym = p.lower = lo;
             RET(phase(p, nullptr));
         }
+    }
+    if (state) {
+        state->r = R.p;
+        state->q = Qc.p;
+        state->ld = R.ld;
+        state->stride = R.stride;
+        state->s = g.s;
     }
     // O = Q X, written in the caller's orientation.
     ProblemSpec p;
@@ -1198,6 +1215,49 @@ int gns_orthogonalize_batched_schedule(float* ptr, int G, int R, int C, int step
     const uint64_t valid = (steps >= 64 ? ~uint64_t(0) : ((uint64_t(1) << steps) - 1)) & ~uint64_t(1);
     if (restart_mask & ~valid) return fail(GNS_ERR_INVALID, "restart mask bits must lie in 1..steps-1");
     return orthogonalize_device(ptr, G, R, C, steps, restart_mask, coeffs, static_cast<cudaStream_t>(stream));
+}
+
+int gns_gram_ns_state(float* ptr, int G, int R, int C, int steps, uint64_t restart_mask, uint16_t* r_state,
+                      uint16_t* q_state, float* r_scale, void* stream) {
+    RET(validate_common(G, R, C, steps));
+    if (G == 0) return GNS_OK;
+    if (!ptr || !r_state || !q_state || !r_scale) return fail(GNS_ERR_INVALID, "null pointer");
+    if (R == C) return fail(GNS_ERR_INVALID, "square matrices run standard Newton-Schulz: no Gram state");
+    const uint64_t valid = (steps >= 64 ? ~uint64_t(0) : ((uint64_t(1) << steps) - 1)) & ~uint64_t(1);
+    if (restart_mask & ~valid) return fail(GNS_ERR_INVALID, "restart mask bits must lie in 1..steps-1");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState* st = nullptr;
+    RET(get_state(&st));
+    begin_call(*st);
+    Coeffs cf;
+    RET(load_coeffs(nullptr, steps, cf));
+    const BucketGeom g = make_geom(R, C);
+    const bool direct_out = (reinterpret_cast<uintptr_t>(ptr) % 16 == 0) && ((static_cast<long long>(C) * 4) % 16 == 0);
+    if (chunk_size(g, G, !direct_out, false) < G) return fail(GNS_ERR_INVALID, "bucket larger than one workspace chunk");
+    const Layout L = make_layout(g, G, !direct_out, false, 0);
+    RET(ensure_workspace(*st, L.total));
+    const long long numel = static_cast<long long>(R) * C;
+    MatrixSet in{ptr, numel, nullptr};
+    OutSpec os;
+    os.out.p = direct_out ? static_cast<void*>(ptr) : static_cast<void*>(st->ws + L.out32);
+    os.out.rows = R;
+    os.out.cols = C;
+    os.out.ld = direct_out ? C : L.ld_out32;
+    os.out.stride = static_cast<long long>(R) * os.out.ld;
+    os.out.f32 = true;
+    GramState gs;
+    RET(run_core(*st, g, L, G, in, nullptr, 0.0f, steps, restart_mask, cf, os, s, &gs));
+    if (!direct_out)
+        LAUNCH(kClsCopy, launch_copy_rows_f32(static_cast<float*>(os.out.p), os.out.ld, os.out.stride, ptr, G, R, C, s));
+    // The matrices of each state are contiguous (stride = n ld), so one 2D
+    // copy per state moves G n rows of n halves.
+    const int n = g.n;
+    CK(cudaMemcpy2DAsync(r_state, static_cast<size_t>(n) * 2, gs.r, static_cast<size_t>(gs.ld) * 2,
+                         static_cast<size_t>(n) * 2, static_cast<size_t>(G) * n, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpy2DAsync(q_state, static_cast<size_t>(n) * 2, gs.q, static_cast<size_t>(gs.ld) * 2,
+                         static_cast<size_t>(n) * 2, static_cast<size_t>(G) * n, cudaMemcpyDeviceToDevice, s));
+    *r_scale = gs.s;
+    return GNS_OK;
 }
 
 int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int steps, int restart_at,
