@@ -1296,27 +1296,41 @@ int gns_orthogonalize_batched_host(float* host_ptr, int G, int R, int C, int ste
     }
     const int gc = static_cast<int>(std::max(1LL, std::min<long long>(G, chunk_bytes / (per * 4))));
     // The first chunk's copy in and the last chunk's orthogonalization and
-    // copy out overlap nothing, so those two chunks are half size; the link
-    // (not the GPU) bounds the rest.
+    // copy out overlap nothing, so the ends taper: a quarter chunk, then the
+    // rest of a chunk, full chunks (a partial one in the middle), the rest of
+    // a chunk and a quarter chunk. The link (not the GPU) bounds the middle.
+    // GNS_HOST_SIZES (comma-separated matrices per chunk, summing to G)
+    // overrides the schedule (tuning).
     std::vector<int> sizes;
-    {
-        int rem = G;
-        if (G > 2 * gc && gc > 1) {
-            const int h = gc / 2;
-            sizes.push_back(h);
-            rem -= 2 * h;
+    if (const char* e = std::getenv("GNS_HOST_SIZES")) {
+        long long sum = 0;
+        for (const char* q = e; *q;) {
+            const long long v = std::atoll(q);
+            if (v <= 0) break;
+            sizes.push_back(static_cast<int>(v));
+            sum += v;
+            while (*q && *q != ',') ++q;
+            if (*q == ',') ++q;
+        }
+        if (sum != G) sizes.clear();
+    }
+    if (sizes.empty()) {
+        auto fill = [&](int rem) {
             while (rem > 0) {
                 const int n = std::min(gc, rem);
                 sizes.push_back(n);
                 rem -= n;
             }
+        };
+        if (G >= 2 * gc && gc > 1) {
+            const int h = std::max(1, gc / 4);
+            sizes.push_back(h);
+            sizes.push_back(gc - h);
+            fill(G - 2 * gc);
+            sizes.push_back(gc - h);
             sizes.push_back(h);
         } else {
-            while (rem > 0) {
-                const int n = std::min(gc, rem);
-                sizes.push_back(n);
-                rem -= n;
-            }
+            fill(G);
         }
     }
     const int nchunks = static_cast<int>(sizes.size());
