@@ -46,7 +46,7 @@ constexpr int BK = 64;
 static_assert(sizeof(GemmProgram) <= 32764, "kernel parameter block too large");
 constexpr int kSchedWarp = 2 + kEpiWarps;     // the scheduler warp follows the epilogue warps
 constexpr int kThreads = 32 * (kSchedWarp + 1);  // producer, MMA, epilogue, scheduler
-constexpr int kRing = 8;                         // tiles the scheduler may run ahead of the slowest role
+constexpr int kRing = 8;                         // ring slots of published tile records (claims are paced by the lookahead)
 
 // Per-warp epilogue shared memory: three 2 KB slots of 32 rows x 64 bytes
 // (64-byte swizzle). Slots 0 and 1 receive, by TMA, the C addend of the
