@@ -594,10 +594,16 @@ def main():
         "effective_tflops": eff * world / per_step_s / 1e12,
         "pct_fp16_peak_algorithmic": 100.0 * alg / per_step_s / 1e12 / peaks["tflops"],
         "pct_fp16_peak_effective": 100.0 * eff / per_step_s / 1e12 / peaks["tflops"],
+        # The GEMM program is timed inside seconds of back-to-back calls under
+        # the power cap, the condition of the sustained peak (a seconds-long
+        # loop of bf16 matmuls); the burst-peak fraction is reported beside it.
         "roofline": {"kernel": "gemm_tc (tcgen05 grouped GEMM, all phases)", "bound": "tensor",
-                     "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
-                     "frac": (achieved / peaks["tflops"]) if achieved else None,
-                     "peak_source": f"{peaks['source']} dense bf16 burst (fp16 rate taken equal)",
+                     "achieved": achieved, "peak": peaks["tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": (achieved / peaks["tflops_sustained"]) if achieved else None,
+                     "peak_source": f"{peaks['source']} dense bf16 sustained (seconds of back-to-back matmuls "
+                                    f"under the power cap; fp16 rate taken equal)",
+                     "peak_burst": peaks["tflops"],
+                     "frac_of_burst": (achieved / peaks["tflops"]) if achieved else None,
                      "launches_per_step": gemm_n / args.steps,
                      "avg_launch_ms": gemm_ms / max(1, gemm_n),
                      "algorithmic_flops_per_launch": alg / max(1e-9, gemm_n / args.steps),
