@@ -318,9 +318,12 @@ __device__ NcItem nc_decode(const NormCastArgs& a, int q) {
 
 template <bool kMomentum>
 __global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_constant__ NormCastArgs a) {
-    __shared__ float red[kThreads / 32];
-    __shared__ int s_next;
-    __shared__ float s_scale;
+    // Per-item shared values, double-buffered by item parity: a block passes
+    // one barrier per item, and a buffer is written again only two items
+    // later, after every thread has passed the barrier in between.
+    __shared__ float red[2][kThreads / 32];
+    __shared__ int s_next[2];
+    __shared__ float s_scale[2];
     grid_dependency_wait();
     grid_launch_dependents();
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -336,12 +339,12 @@ __global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_con
             pending = -1;
         }
     };
-    if (t == 0) s_next = atomicAdd(ticket, 1);
+    if (t == 0) s_next[0] = atomicAdd(ticket, 1);
     __syncthreads();
-    int q = s_next;
-    while (q < a.total) {
-        __syncthreads();  // every thread has read s_next
-        // The next ticket is taken now; its value is needed only at the end.
+    int q = s_next[0];
+    for (int k = 0; q < a.total; ++k) {
+        const int b = k & 1;
+        // The next ticket is taken now; its value is needed only at the barrier.
         int nxt = 0;
         if (t == 0) nxt = atomicAdd(ticket, 1);
         const NcItem it = nc_decode(a, q);
@@ -362,13 +365,14 @@ __global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_con
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) red[warp] = s;
-            // The barrier also orders every thread's M stores (momentum) before
-            // thread 0's release.
+            if (lane == 0) red[b][warp] = s;
+            if (t == 0) s_next[b ^ 1] = nxt;
+            // The item's one barrier; it also orders every thread's M stores
+            // (momentum) before thread 0's release at its next item.
             __syncthreads();
             if (t == 0) {
                 float v = 0.0f;
-                for (int w = 0; w < kThreads / 32; ++w) v += red[w];
+                for (int w = 0; w < kThreads / 32; ++w) v += red[b][w];
                 a.j.partial[static_cast<long long>(it.g) * a.nparts + it.part] = v;
                 pending = it.g;
             }
@@ -394,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_con
                         float pv[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            const int b = b0 + lane + 32 * u;
-                            pv[u] = b < a.nparts ? __ldcg(p + b) : 0.0f;
+                            const int bb = b0 + lane + 32 * u;
+                            pv[u] = bb < a.nparts ? __ldcg(p + bb) : 0.0f;
                         }
 #pragma unroll
                         for (int u = 0; u < 8; ++u) v += pv[u];
@@ -406,18 +410,17 @@ __global__ void __launch_bounds__(kThreads, 2) norm_cast_kernel(const __grid_con
                 if (lane == 0) {
                     const float norm = sqrtf(v);
                     if (ok && !isfinite(norm)) raise_error(a.j.st, kDevErrNonFinite);
-                    s_scale = ok ? ldexpf(1.0f, a.j.k_exp) / (1.05f * (norm + 1e-7f)) : 0.0f;
+                    s_scale[b] = ok ? ldexpf(1.0f, a.j.k_exp) / (1.05f * (norm + 1e-7f)) : 0.0f;
                 }
             }
-            __syncthreads();
+            if (t == 0) s_next[b ^ 1] = nxt;
+            __syncthreads();  // the item's one barrier: the scale and the next ticket
             if constexpr (kMomentum) item_load(regs, x, beg, end);
-            item_cast_store(regs, x, beg, end, a.j.C, s_scale,
+            item_cast_store(regs, x, beg, end, a.j.C, s_scale[b],
                             static_cast<__half*>(a.j.out) + static_cast<long long>(it.g) * a.j.stride_out,
                             a.j.ld_out);
         }
-        if (t == 0) s_next = nxt;
-        __syncthreads();
-        q = s_next;
+        q = s_next[b ^ 1];
     }
     release_pending();
 }
