@@ -58,6 +58,12 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert lib.gns_muon_update(vp(0), vp(0), 4, 4, 0.1, 0.0, 1.0, 0, 0, -1, vp(0)) == -1
     assert lib.muon_step(None, None, None, -1, 0.1, 0.0, 0.9, 0, 0, vp(0)) == -1
     assert lib.muon_step(None, None, None, 0, 0.1, 0.0, 0.9, 0, 0, vp(0)) == 0
+    scale = ctypes.c_float(0.0)
+    # Gram-state entry: square matrices have no Gram state; mask bits only in 1 .. steps - 1.
+    assert lib.gns_gram_ns_state(vp(16), 1, 8, 8, 5, 4, vp(16), vp(16), ctypes.byref(scale), vp(0)) == -1
+    assert lib.gns_gram_ns_state(vp(16), 1, 8, 16, 5, 1 << 5, vp(16), vp(16), ctypes.byref(scale), vp(0)) == -1
+    assert lib.gns_gram_ns_state(vp(16), 1, 8, 16, 5, 1, vp(16), vp(16), ctypes.byref(scale), vp(0)) == -1
+    assert lib.gns_gram_ns_state(vp(16), 1, 8, 16, 5, 4, vp(0), vp(16), ctypes.byref(scale), vp(0)) == -1
     assert lib.gns_last_error().decode() != ""
 
 
