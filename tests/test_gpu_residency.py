@@ -133,3 +133,19 @@ def test_results_independent_of_grid_size(gns, tmp_path):
     assert len(small.files) == len(full)
     for i, a in enumerate(full):
         assert np.array_equal(small[f"arr_{i}"], a), f"output {i} differs between grid sizes"
+
+
+def test_results_independent_of_claim_pacing(gns, monkeypatch):
+    """How far ahead of its producer a pair claims tiles (GNS_LOOKAHEAD)
+    changes which pair computes which tile, never a tile's arithmetic: the
+    outputs are bitwise equal for lookaheads 1, 3 and 8."""
+    X = gen.gaussian_bucket(10, 1024, 2048, seed=7400)
+    outs = {}
+    for la in ("1", "3", "8"):
+        monkeypatch.setenv("GNS_LOOKAHEAD", la)
+        t = torch.from_numpy(np.ascontiguousarray(X, dtype=np.float32)).cuda()
+        gns.gns_orthogonalize_batched(t)
+        torch.cuda.synchronize()
+        assert gns.gns_get_status() == 0
+        outs[la] = t.cpu().numpy()
+    assert np.array_equal(outs["1"], outs["3"]) and np.array_equal(outs["1"], outs["8"])
